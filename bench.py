@@ -1,0 +1,405 @@
+#!/usr/bin/env python3
+"""Benchmark of UniPrefill block scoring + top-p selection + compaction on GB300.
+
+One step = one pass of the whole hot path (up_score_blocks, up_select_topp,
+up_compact) over one batch of synthetic Llama-3.1-8B-layer-shaped input
+(default: one 131072-token sequence, 32 query / 8 KV heads, head_dim 128,
+hidden 4096, n = 128, G = 64, p = 0.99).  Inputs are resident in HBM when the
+timed region starts; k (268 MB) and x (1.07 GB) are larger than the 129 MB L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank processes its own copy of the batch (the
+path shards by sequence; there is no data-path collective): weak scaling.
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "scored+compacted prefill tokens/s at N=128K Llama-8B shape; % of roofline"
+UNIT = "tokens/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama31_8b_128k")
+    ap.add_argument("--gain", default="5", help="logit gain of the planted shifts, or 'literal'")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def gain_of(s):
+    return None if s == "literal" else float(s)
+
+
+# ---------------------------------------------------------------- work model
+
+def valid_pairs(inp):
+    """Visible (query, key) pairs per query head: sum_s n_s*L_s - n_s(n_s-1)/2."""
+    tot = 0
+    for s in range(inp.num_seqs):
+        L = int(inp.cu_seqlens[s + 1] - inp.cu_seqlens[s])
+        ns = min(inp.n, L)
+        tot += ns * L - ns * (ns - 1) // 2
+    return tot
+
+
+def work_model(inp, G):
+    pairs = valid_pairs(inp)
+    flops = 2.0 * inp.d * inp.Hq * pairs
+    exps = float(inp.Hq * pairs)
+    nb = sum((int(inp.cu_seqlens[s + 1] - inp.cu_seqlens[s]) + G - 1) // G
+             for s in range(inp.num_seqs))
+    score_bytes = inp.k.nbytes + inp.q_last.nbytes + 4 * nb + 4 * (inp.num_seqs + 1)
+    return dict(flops=flops, exps=exps, score_bytes=score_bytes, blocks=nb)
+
+
+def compact_bytes(kept_tokens, hidden):
+    # x rows read + written, positions read + written
+    return kept_tokens * (2 * 2 * hidden + 8)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id:
+            cmd.insert(1, f"--id={gpu_id}")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(inp, heads, queries, threads, G, p):
+    """Time the fp64 oracle on a sample: the first `heads` query heads (with
+    their KV heads) and the last `queries` queries of every sequence, over all
+    keys, then top-p and compaction of the result.  Returns (seconds, fraction
+    of the full workload's scoring work)."""
+    import oracle
+    g = inp.Hq // inp.Hk
+    hs = max(1, min(heads, inp.Hq))
+    kv = (hs + g - 1) // g
+    hs = min(inp.Hq, kv * g) if hs > g else hs
+    nq = max(1, min(queries, inp.n))
+    rows, qsel = [], []
+    off = 0
+    for s in range(inp.num_seqs):
+        L = int(inp.cu_seqlens[s + 1] - inp.cu_seqlens[s])
+        ns = min(inp.n, L)
+        keep_q = min(nq, ns)
+        qsel.append(inp.q_last[off + ns - keep_q: off + ns, :hs])
+        rows.append(keep_q)
+        off += ns
+    q = np.ascontiguousarray(np.concatenate(qsel, axis=0))
+    k = np.ascontiguousarray(inp.k[:, :kv])
+    t0 = time.perf_counter()
+    sc, cb = oracle.score_blocks(q, k, inp.cu_seqlens, hs, kv, inp.d, nq, G, nthreads=threads)
+    keep, _, _, _ = oracle.select_topp(sc, cb, inp.cu_seqlens, G, p)
+    oracle.compact(inp.x, inp.pos, inp.cu_seqlens, G, keep, cb, with_x=inp.x is not None)
+    dt = time.perf_counter() - t0
+    full_rows = sum(min(inp.n, int(inp.cu_seqlens[s + 1] - inp.cu_seqlens[s]))
+                    for s in range(inp.num_seqs)) * inp.Hq
+    frac = (sum(rows) * hs) / max(1, full_rows)
+    return dt, frac, hs, nq
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, inp, w):
+    """--impl reference: the oracle, as it stands, on the host cores."""
+    cores = cpu_cores()
+    threads = cores
+    budget = 150.0 / max(1, args.steps + args.warmup)  # seconds per step
+    # calibrate on one query of one head
+    dt1, frac1, _, _ = oracle_sample(inp, 1, 1, 1, w["G"], w["p"])
+    per_row = max(dt1, 1e-4)
+    rows_fit = max(1, int(budget * min(threads, inp.Hq) / per_row))
+    heads = min(inp.Hq, max(1, rows_fit // inp.n))
+    queries = inp.n if heads > 1 else max(1, min(inp.n, rows_fit))
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, frac, hs, nq = oracle_sample(inp, heads, queries, threads, w["G"], w["p"])
+        if i >= args.warmup:
+            times.append(dt)
+    t = sum(times) / len(times)
+    value = inp.total_tokens * frac / t
+    used = min(threads, hs)
+    sample = (f"{hs} of {inp.Hq} query heads x last {nq} of {inp.n} queries over all "
+              f"{inp.total_tokens} keys per step (fraction {frac:.4g} of the scoring work), "
+              f"value scaled to the full workload")
+    return dict(metric=METRIC, value=value, unit=UNIT, impl="reference", n_gpus=args.gpus,
+                steps=args.steps, warmup=args.warmup, ms_per_step=t * 1e3 / frac,
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic", config=dict(workload=args.workload, gain=args.gain),
+                cpu_baseline=dict(value=value, unit=UNIT, cores=used, kind="oracle",
+                                  sample=sample),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args, inp, w, rank, world):
+    import torch
+    import block_sparse_long_up_gb300 as up
+
+    up.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    G, p, n = w["G"], w["p"], inp.n
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    h_q = bf16(inp.q_last).pin_memory()
+    h_k = bf16(inp.k).pin_memory()
+    h_x = bf16(inp.x).pin_memory()
+    h_cu = torch.from_numpy(inp.cu_seqlens).pin_memory()
+    h_pos = torch.from_numpy(inp.pos).pin_memory()
+    q, k, x = h_q.to(dev), h_k.to(dev), h_x.to(dev)
+    cu, pos = h_cu.to(dev), h_pos.to(dev)
+    sp = up.Sparsifier(inp.num_seqs, inp.total_tokens, inp.Hq, inp.Hk, inp.d, inp.hidden, n, G, p,
+                       device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        sp.run(q, k, cu, x, pos)
+    torch.cuda.synchronize()
+    if up.get_device_error():
+        raise RuntimeError("device error during warm-up")
+    kept = int(sp.total_kept.item())
+    kept_blocks = int(sp.keep[: int(sp.cu_blocks[-1].item())].sum().item())
+
+    # timed region: K steps; per-call events on the launching stream
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_uuid)
+    start.record(stream)
+    for i in range(K):
+        e = ev[i]
+        e[0].record(stream)
+        up.score_blocks(q, k, cu, n, G, sp.scores, sp.cu_blocks, sp.ws_score)
+        e[1].record(stream)
+        up.select_topp(sp.scores, sp.cu_blocks, cu, G, p, sp.keep, sp.kept_tokens)
+        e[2].record(stream)
+        up.compact(x, pos, cu, G, sp.keep, sp.cu_blocks, sp.x_out, sp.pos_out, sp.cu_out,
+                   sp.src_idx, sp.total_kept, sp.ws_compact)
+        e[3].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms_total = start.elapsed_time(end)
+    ms_step = max_over_ranks(ms_total / K, world)
+    t_score = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    t_select = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    t_compact = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    if up.get_device_error():
+        raise RuntimeError("device error during the timed region")
+
+    # end to end: host (pinned) inputs -> device, the three calls, result -> host
+    E = max(1, args.e2e_steps)
+    h_total = torch.empty(1, dtype=torch.int32).pin_memory()
+    h_cuo = torch.empty(inp.num_seqs + 1, dtype=torch.int32).pin_memory()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(E):
+        q.copy_(h_q, non_blocking=True)
+        k.copy_(h_k, non_blocking=True)
+        x.copy_(h_x, non_blocking=True)
+        cu.copy_(h_cu, non_blocking=True)
+        pos.copy_(h_pos, non_blocking=True)
+        sp.run(q, k, cu, x, pos)
+        h_total.copy_(sp.total_kept, non_blocking=True)
+        h_cuo.copy_(sp.cu_out, non_blocking=True)
+        torch.cuda.synchronize()
+        assert int(h_total[0]) == kept
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / E, world)
+    h2d = h_q.nbytes + h_k.nbytes + h_x.nbytes + h_cu.nbytes + h_pos.nbytes
+    d2h = h_total.nbytes + h_cuo.nbytes
+
+    wm = work_model(inp, G)
+    peaks, peak_src = measured_peaks()
+    tc_peak = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
+    achieved = wm["flops"] / (t_score * 1e-3) / 1e12
+    cbytes = compact_bytes(kept, inp.hidden)
+    value = world * inp.total_tokens / (ms_step * 1e-3)
+    out = dict(
+        metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=K, warmup=args.warmup,
+        ms_per_step=ms_step, higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="bf16", data="synthetic",
+        config=dict(workload=args.workload, tokens=inp.total_tokens, num_seqs=inp.num_seqs,
+                    Hq=inp.Hq, Hk=inp.Hk, head_dim=inp.d, hidden=inp.hidden, n=n, G=G, p=p,
+                    gain=args.gain, parallelism=f"replica x{world}" if world > 1 else "single",
+                    l2="inputs larger than L2 (k %.0f MB, x %.0f MB > 129 MB); no flush"
+                       % (inp.k.nbytes / 1e6, inp.x.nbytes / 1e6)),
+        clocks=clk,
+        e2e=dict(value=world * inp.total_tokens / e2e_s, unit=UNIT, h2d_bytes_per_step=h2d,
+                 d2h_bytes_per_step=d2h, ms_per_step=e2e_s * 1e3),
+        gpu_launches=K * sp.launches_per_step(),
+        roofline=dict(kernel="up_score_blocks", bound="tensor", achieved=achieved, peak=tc_peak,
+                      unit="TFLOP/s", frac=achieved / tc_peak, traffic=None,
+                      peak_source=f"{peak_src} bf16 sustained",
+                      exp_rate_per_s=wm["exps"] / (t_score * 1e-3)),
+        calls_ms=dict(score=t_score, select=t_select, compact=t_compact),
+        compact_roofline=dict(bound="hbm", achieved=cbytes / (t_compact * 1e-3) / 1e9,
+                              peak=float(peaks["hbm_gbs"]), unit="GB/s",
+                              frac=cbytes / (t_compact * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
+                              bytes=cbytes),
+        kept=dict(tokens=kept, blocks=kept_blocks, blocks_total=wm["blocks"],
+                  rho=kept / inp.total_tokens),
+    )
+    return out
+
+
+def main():
+    args = parse_args()
+    from block_sparse_long_up_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        inp = synth.make_workload(args.workload, gain=gain_of(args.gain))
+        out = run_reference(args, inp, w)
+        out["n_gpus"] = world
+        print(json.dumps(out), flush=True)
+        return 0
+    rank, world = dist_setup()
+    inp = synth.make_workload(args.workload, gain=gain_of(args.gain))
+    out = run_ours(args, inp, w, rank, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            cores = cpu_cores()
+            threads = min(cores, 8)
+            dt, frac, hs, nq = oracle_sample(inp, 8, inp.n, threads, w["G"], w["p"])
+            out["cpu_baseline"] = dict(
+                value=inp.total_tokens * frac / dt, unit=UNIT, cores=min(threads, hs),
+                kind="oracle",
+                sample=f"{hs} of {inp.Hq} query heads x {nq} queries over all {inp.total_tokens} "
+                       f"keys (fraction {frac:.4g} of the scoring work) plus top-p and "
+                       f"compaction; tokens/s scaled to the full workload")
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

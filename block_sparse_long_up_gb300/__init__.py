@@ -1,0 +1,230 @@
+"""UniPrefill block-wise sparsification hot path for GB300 (sm_103a).
+
+A thin ctypes binding over ``libup.so`` (see include/up.h): the functions here
+check tensor dtypes/devices, allocate outputs with PyTorch and pass raw device
+pointers and the current CUDA stream to the C ABI.  Every step of the path runs
+in the library's CUDA kernels; there is no Python or CPU compute path.  If the
+library is not built, every call raises.
+
+    scores, cu_blocks = score_blocks(q_last, k, cu_seqlens, n, G)
+    keep, kept_tokens = select_topp(scores, cu_blocks, cu_seqlens, G, p)
+    x_out, pos_out, cu_out, total = compact(x, pos, cu_seqlens, G, keep, cu_blocks)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = ["build", "lib", "UpError", "score_blocks_workspace", "score_blocks", "select_topp",
+           "compact_workspace", "compact", "get_device_error", "Sparsifier", "SELECT_MAX_BLOCKS"]
+
+SELECT_MAX_BLOCKS = 16384
+_lib = None
+
+
+class UpError(RuntimeError):
+    def __init__(self, where, status):
+        msg = lib().up_status_string(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+def build(force: bool = False) -> str:
+    """Compile libup.so for sm_103a (nvcc) into the package's _build/ folder."""
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded libup.so (ctypes).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"{_build.LIB} is missing: build it with block_sparse_long_up_gb300.build()")
+    L = ctypes.CDLL(_build.LIB)
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    L.up_status_string.argtypes = [I]
+    L.up_status_string.restype = ctypes.c_char_p
+    L.up_score_blocks_workspace.argtypes = [I, I64, I, I, I, I, I]
+    L.up_score_blocks_workspace.restype = SZ
+    L.up_score_blocks.argtypes = [P, P, P, I, I64, I, I, I, I, I, P, P, P, SZ, P]
+    L.up_score_blocks.restype = I
+    L.up_select_topp.argtypes = [P, P, P, I, I, ctypes.c_double, P, P, P]
+    L.up_select_topp.restype = I
+    L.up_compact_workspace.argtypes = [I, I64, I]
+    L.up_compact_workspace.restype = SZ
+    L.up_compact.argtypes = [P, P, I, P, I, I64, I, P, P, P, P, P, P, P, P, SZ, P]
+    L.up_compact.restype = I
+    L.up_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.up_get_device_error.restype = I
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _check(where, status):
+    if status != 0:
+        raise UpError(where, status)
+
+
+def _alloc_ws(nbytes, device):
+    # 256-byte alignment comes with the caching allocator's blocks
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def score_blocks_workspace(num_seqs, total_tokens, Hq, Hk, d, n, G) -> int:
+    return int(lib().up_score_blocks_workspace(num_seqs, total_tokens, Hq, Hk, d, n, G))
+
+
+def score_blocks(q_last, k, cu_seqlens, n, G, scores=None, cu_blocks=None, workspace=None,
+                 stream=None):
+    """Block scores (fp32 [sum nb_s]) and cu_blocks (int32 [B+1]); see up_score_blocks."""
+    _need(k, "k", torch.bfloat16)
+    dev = k.device
+    _need(q_last, "q_last", torch.bfloat16, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    total, Hk, d = k.shape
+    Hq = q_last.shape[1]
+    B = cu_seqlens.numel() - 1
+    cap = total // G + B
+    if scores is None:
+        scores = torch.empty(max(cap, 1), dtype=torch.float32, device=dev)
+    if cu_blocks is None:
+        cu_blocks = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    _need(scores, "scores", torch.float32, dev)
+    _need(cu_blocks, "cu_blocks", torch.int32, dev)
+    if scores.numel() < cap:
+        raise ValueError(f"scores needs {cap} entries")
+    ws_need = score_blocks_workspace(B, total, Hq, Hk, d, n, G)
+    if workspace is None:
+        workspace = _alloc_ws(ws_need, dev)
+    st = lib().up_score_blocks(_ptr(q_last), _ptr(k), _ptr(cu_seqlens), B, total, Hq, Hk, d, n,
+                               G, _ptr(scores), _ptr(cu_blocks), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("up_score_blocks", st)
+    return scores, cu_blocks
+
+
+def select_topp(scores, cu_blocks, cu_seqlens, G, p, keep=None, kept_tokens=None, stream=None):
+    """Top-p keep flags (uint8 [sum nb_s]) and kept tokens per sequence (int32 [B])."""
+    _need(scores, "scores", torch.float32)
+    dev = scores.device
+    _need(cu_blocks, "cu_blocks", torch.int32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    B = cu_seqlens.numel() - 1
+    if keep is None:
+        keep = torch.empty(max(scores.numel(), 1), dtype=torch.uint8, device=dev)
+    if kept_tokens is None:
+        kept_tokens = torch.empty(max(B, 1), dtype=torch.int32, device=dev)
+    _need(keep, "keep", torch.uint8, dev)
+    _need(kept_tokens, "kept_tokens", torch.int32, dev)
+    st = lib().up_select_topp(_ptr(scores), _ptr(cu_blocks), _ptr(cu_seqlens), B, G, float(p),
+                              _ptr(keep), _ptr(kept_tokens), _stream(stream))
+    _check("up_select_topp", st)
+    return keep, kept_tokens
+
+
+def compact_workspace(num_seqs, total_tokens, G) -> int:
+    return int(lib().up_compact_workspace(num_seqs, total_tokens, G))
+
+
+def compact(x, pos, cu_seqlens, G, keep, cu_blocks, x_out=None, pos_out=None,
+            cu_seqlens_out=None, src_idx=None, total_kept=None, workspace=None, stream=None,
+            want_src_idx=True):
+    """Gather kept rows.  Outputs are sized for keeping everything; the true
+    row count is total_kept (int32 [1], on the device)."""
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    _need(pos, "pos", torch.int32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _need(keep, "keep", torch.uint8, dev)
+    _need(cu_blocks, "cu_blocks", torch.int32, dev)
+    total, hidden = x.shape
+    B = cu_seqlens.numel() - 1
+    if x_out is None:
+        x_out = torch.empty(max(total, 1), hidden, dtype=torch.bfloat16, device=dev)
+    if pos_out is None:
+        pos_out = torch.empty(max(total, 1), dtype=torch.int32, device=dev)
+    if cu_seqlens_out is None:
+        cu_seqlens_out = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    if src_idx is None and want_src_idx:
+        src_idx = torch.empty(max(total, 1), dtype=torch.int32, device=dev)
+    if total_kept is None:
+        total_kept = torch.empty(1, dtype=torch.int32, device=dev)
+    if x_out.shape[0] < total or pos_out.numel() < total:
+        raise ValueError("x_out/pos_out must hold total_tokens rows")
+    ws_need = compact_workspace(B, total, G)
+    if workspace is None:
+        workspace = _alloc_ws(ws_need, dev)
+    st = lib().up_compact(_ptr(x), _ptr(pos), hidden, _ptr(cu_seqlens), B, total, G, _ptr(keep),
+                          _ptr(cu_blocks), _ptr(x_out), _ptr(pos_out), _ptr(cu_seqlens_out),
+                          _ptr(src_idx), _ptr(total_kept), _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("up_compact", st)
+    return x_out, pos_out, cu_seqlens_out, total_kept, src_idx
+
+
+def get_device_error() -> int:
+    """Read and clear the library's sticky device error bits (synchronises the device)."""
+    v = ctypes.c_uint32(0)
+    lib().up_get_device_error(ctypes.byref(v))
+    return int(v.value)
+
+
+class Sparsifier:
+    """Preallocated buffers for repeated score -> select -> compact passes over
+    batches of one shape (the three C-ABI calls, in order, on one stream)."""
+
+    def __init__(self, num_seqs, total_tokens, Hq, Hk, d, hidden, n, G, p, device="cuda"):
+        dev = torch.device(device)
+        self.num_seqs, self.total, self.n, self.G, self.p = num_seqs, total_tokens, n, G, p
+        cap = total_tokens // G + num_seqs
+        self.scores = torch.empty(max(cap, 1), dtype=torch.float32, device=dev)
+        self.cu_blocks = torch.empty(num_seqs + 1, dtype=torch.int32, device=dev)
+        self.keep = torch.empty(max(cap, 1), dtype=torch.uint8, device=dev)
+        self.kept_tokens = torch.empty(max(num_seqs, 1), dtype=torch.int32, device=dev)
+        self.x_out = torch.empty(max(total_tokens, 1), hidden, dtype=torch.bfloat16, device=dev)
+        self.pos_out = torch.empty(max(total_tokens, 1), dtype=torch.int32, device=dev)
+        self.cu_out = torch.empty(num_seqs + 1, dtype=torch.int32, device=dev)
+        self.src_idx = torch.empty(max(total_tokens, 1), dtype=torch.int32, device=dev)
+        self.total_kept = torch.empty(1, dtype=torch.int32, device=dev)
+        self.ws_score = _alloc_ws(score_blocks_workspace(num_seqs, total_tokens, Hq, Hk, d, n, G), dev)
+        self.ws_compact = _alloc_ws(compact_workspace(num_seqs, total_tokens, G), dev)
+
+    def launches_per_step(self) -> int:
+        # score: plan, main, finalize rows, finalize blocks; select: 1; compact: index, gather
+        return (4 if self.total > 0 and self.num_seqs > 0 else 1) + 1 + 2
+
+    def run(self, q_last, k, cu_seqlens, x, pos, stream=None):
+        score_blocks(q_last, k, cu_seqlens, self.n, self.G, self.scores, self.cu_blocks,
+                     self.ws_score, stream)
+        select_topp(self.scores, self.cu_blocks, cu_seqlens, self.G, self.p, self.keep,
+                    self.kept_tokens, stream)
+        compact(x, pos, cu_seqlens, self.G, self.keep, self.cu_blocks, self.x_out, self.pos_out,
+                self.cu_out, self.src_idx, self.total_kept, self.ws_compact, stream)
+        return self.total_kept

@@ -1,0 +1,263 @@
+// api.cu -- the C ABI declared in include/up.h: argument validation, workspace
+// layout, per-device state and kernel launches.  No compute happens here.
+#include <mutex>
+
+#include "../../include/up.h"
+#include "common.cuh"
+
+namespace {
+
+// Sticky device error word (UP_DEVERR_* bits), one per device.
+__device__ unsigned int g_up_device_error;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    unsigned int *err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+up_status device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return UP_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return UP_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_up_device_error) != cudaSuccess) return UP_ERR_CUDA;
+        d.err = static_cast<unsigned int *>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return UP_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+bool valid_G(int G) { return G == 16 || G == 32 || G == 64 || G == 128 || G == 256; }
+bool valid_d(int d) { return d == 64 || d == 128 || d == 256; }
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Keys per work unit.  A function of the call's shape only (not of the GPU),
+// so scores are reproducible across devices: the largest power of two in
+// [256, 4096] that still yields >= 1024 work units.
+int choose_chunk(int B, int64_t total, int Hq, int Hk, int n) {
+    const int g = Hq / Hk;
+    const int64_t nn = n < total ? n : total;
+    const int64_t mt = (int64_t)Hk * ((g * nn + up::kRowsPerTile - 1) / up::kRowsPerTile);
+    (void)B;
+    for (int C = 4096; C > up::kChunkQuantum; C >>= 1)
+        if (mt * (total / C) >= 1024) return C;
+    return up::kChunkQuantum;
+}
+
+up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int n, int G) {
+    up::ScoreLayout L{};
+    const int g = Hq / Hk;
+    L.chunk = choose_chunk(B, total, Hq, Hk, n);
+    const int64_t nn = n < total ? n : total;
+    const int64_t ns_sum = ((int64_t)n * B < total) ? (int64_t)n * B : total;
+    L.max_blocks = total / G + B;
+    L.max_rows = (int64_t)Hq * ns_sum;
+    L.max_part = (int64_t)Hq * nn * L.max_blocks;
+    const int64_t max_chunks = total / L.chunk + B;
+    L.max_stat = (int64_t)Hq * nn * max_chunks;
+    L.max_units = (int64_t)Hk * ((g * nn + up::kRowsPerTile - 1) / up::kRowsPerTile) * max_chunks;
+    size_t off = 0;
+    L.seqs = off;     off = align256(off + sizeof(up::SeqInfo) * (size_t)(B > 0 ? B : 1));
+    L.counters = off; off = align256(off + sizeof(up::Counters));
+    L.part = off;     off = align256(off + sizeof(float) * (size_t)L.max_part);
+    L.mref = off;     off = align256(off + sizeof(float) * (size_t)L.max_stat);
+    L.lsum = off;     off = align256(off + sizeof(float) * (size_t)L.max_stat);
+    L.w = off;        off = align256(off + sizeof(float) * (size_t)L.max_stat);
+    L.total = off;
+    return L;
+}
+
+struct CompactLayout {
+    size_t nkept, list, dst_blk, total;
+};
+
+CompactLayout compact_layout(int B, int64_t total, int G) {
+    CompactLayout L{};
+    const int64_t max_blocks = total / G + B;
+    size_t off = 0;
+    L.nkept = off;   off = align256(off + 256);
+    L.list = off;    off = align256(off + sizeof(int4) * (size_t)(max_blocks > 0 ? max_blocks : 1));
+    L.dst_blk = off; off = align256(off + sizeof(int32_t) * (size_t)(max_blocks > 0 ? max_blocks : 1));
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *up_status_string(up_status status) {
+    switch (status) {
+        case UP_OK: return "ok";
+        case UP_ERR_INVALID_ARG: return "invalid argument";
+        case UP_ERR_UNSUPPORTED: return "unsupported configuration";
+        case UP_ERR_WORKSPACE: return "workspace missing or too small";
+        case UP_ERR_CUDA: return "CUDA error";
+        case UP_ERR_TIMEOUT: return "device-side bounded wait expired";
+        case UP_ERR_DEVICE: return "device-side argument check failed";
+    }
+    return "unknown status";
+}
+
+up_status up_get_device_error(uint32_t *bits) {
+    if (!bits) return UP_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    up_status st = device_state(&ds);
+    if (st != UP_OK) return st;
+    unsigned int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return UP_ERR_CUDA;
+    if (cudaMemcpy(&v, ds->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return UP_ERR_CUDA;
+    if (cudaMemset(ds->err, 0, sizeof v) != cudaSuccess) return UP_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return UP_ERR_CUDA;
+    *bits = v;
+    if (v & UP_DEVERR_TIMEOUT) return UP_ERR_TIMEOUT;
+    return v ? UP_ERR_DEVICE : UP_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+up_status check_score_args(const void *q_last, const void *k, const int32_t *cu_seqlens,
+                           int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
+                           int G, const float *scores, const int32_t *cu_blocks) {
+    if (num_seqs < 0 || total_tokens < 0 || total_tokens > INT32_MAX) return UP_ERR_INVALID_ARG;
+    if (!cu_seqlens || !cu_blocks) return UP_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q_last || !k || !scores)) return UP_ERR_INVALID_ARG;
+    if (Hq < 1 || Hk < 1 || Hq % Hk != 0 || n < 1 || d < 1 || G < 1) return UP_ERR_INVALID_ARG;
+    if (Hq / Hk > 16 || !valid_d(d) || !valid_G(G) || n > 1024) return UP_ERR_UNSUPPORTED;
+    if (!aligned(q_last, 16) || !aligned(k, 16) || !aligned(scores, 4)) return UP_ERR_INVALID_ARG;
+    return UP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t up_score_blocks_workspace(int num_seqs, int64_t total_tokens, int Hq, int Hk, int d,
+                                 int n, int G) {
+    if (check_score_args(reinterpret_cast<const void *>(16), reinterpret_cast<const void *>(16),
+                         reinterpret_cast<const int32_t *>(16), num_seqs, total_tokens, Hq, Hk,
+                         d, n, G, reinterpret_cast<const float *>(16),
+                         reinterpret_cast<const int32_t *>(16)) != UP_OK)
+        return 0;
+    return score_layout(num_seqs, total_tokens, Hq, Hk, n, G).total;
+}
+
+up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_seqlens,
+                          int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
+                          int G, float *scores, int32_t *cu_blocks, void *workspace,
+                          size_t workspace_bytes, up_stream_t stream) {
+    up_status st = check_score_args(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n,
+                                    G, scores, cu_blocks);
+    if (st != UP_OK) return st;
+    const up::ScoreLayout lay = score_layout(num_seqs, total_tokens, Hq, Hk, n, G);
+    if (!workspace || workspace_bytes < lay.total || !aligned(workspace, 256))
+        return UP_ERR_WORKSPACE;
+    DeviceState *ds = nullptr;
+    if ((st = device_state(&ds)) != UP_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    up::ScoreParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q_last);
+    p.k = static_cast<const __nv_bfloat16 *>(k);
+    p.seqs = reinterpret_cast<const up::SeqInfo *>(ws + lay.seqs);
+    p.counters = reinterpret_cast<const up::Counters *>(ws + lay.counters);
+    p.part = reinterpret_cast<float *>(ws + lay.part);
+    p.mref = reinterpret_cast<float *>(ws + lay.mref);
+    p.lsum = reinterpret_cast<float *>(ws + lay.lsum);
+    p.w = reinterpret_cast<float *>(ws + lay.w);
+    p.scores = scores;
+    p.num_seqs = num_seqs;
+    p.Hq = Hq; p.Hk = Hk; p.g = Hq / Hk; p.d = d; p.n = n; p.G = G; p.C = lay.chunk;
+    p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
+    p.err = ds->err;
+    if (up::launch_score_plan(cu_seqlens, cu_blocks, p, total_tokens, s) != cudaSuccess)
+        return UP_ERR_CUDA;
+    if (num_seqs == 0 || total_tokens == 0) return UP_OK;
+    if (up::launch_score_main(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
+    if (up::launch_score_finalize(p, lay, s) != cudaSuccess) return UP_ERR_CUDA;
+    return UP_OK;
+}
+
+up_status up_select_topp(const float *scores, const int32_t *cu_blocks,
+                         const int32_t *cu_seqlens, int num_seqs, int G, double p,
+                         uint8_t *keep, int32_t *kept_tokens, up_stream_t stream) {
+    if (num_seqs < 0 || G < 1 || !(p > 0.0)) return UP_ERR_INVALID_ARG;
+    if (!valid_G(G)) return UP_ERR_UNSUPPORTED;
+    if (num_seqs > 0 && (!scores || !cu_blocks || !cu_seqlens || !keep || !kept_tokens))
+        return UP_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    up_status st = device_state(&ds);
+    if (st != UP_OK) return st;
+    if (up::launch_select(scores, cu_blocks, cu_seqlens, num_seqs, G, p, keep, kept_tokens,
+                          ds->err, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return UP_ERR_CUDA;
+    return UP_OK;
+}
+
+size_t up_compact_workspace(int num_seqs, int64_t total_tokens, int G) {
+    if (num_seqs < 0 || total_tokens < 0 || total_tokens > INT32_MAX || !valid_G(G)) return 0;
+    return compact_layout(num_seqs, total_tokens, G).total;
+}
+
+up_status up_compact(const void *x, const int32_t *pos, int hidden, const int32_t *cu_seqlens,
+                     int num_seqs, int64_t total_tokens, int G, const uint8_t *keep,
+                     const int32_t *cu_blocks, void *x_out, int32_t *pos_out,
+                     int32_t *cu_seqlens_out, int32_t *src_idx, int32_t *total_kept,
+                     void *workspace, size_t workspace_bytes, up_stream_t stream) {
+    if (num_seqs < 0 || total_tokens < 0 || total_tokens > INT32_MAX || hidden < 1 || G < 1)
+        return UP_ERR_INVALID_ARG;
+    if (!valid_G(G)) return UP_ERR_UNSUPPORTED;
+    if (hidden % 8 != 0) return UP_ERR_UNSUPPORTED;
+    if (!cu_seqlens || !cu_blocks || !cu_seqlens_out || !total_kept) return UP_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!x || !pos || !keep || !x_out || !pos_out)) return UP_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(x_out, 16)) return UP_ERR_INVALID_ARG;
+    const CompactLayout lay = compact_layout(num_seqs, total_tokens, G);
+    if (!workspace || workspace_bytes < lay.total || !aligned(workspace, 256))
+        return UP_ERR_WORKSPACE;
+    DeviceState *ds = nullptr;
+    up_status st = device_state(&ds);
+    if (st != UP_OK) return st;
+    char *ws = static_cast<char *>(workspace);
+    up::CompactArgs a{};
+    a.x = static_cast<const uint4 *>(x);
+    a.pos = pos;
+    a.cu_seqlens = cu_seqlens;
+    a.keep = keep;
+    a.cu_blocks = cu_blocks;
+    a.x_out = static_cast<uint4 *>(x_out);
+    a.pos_out = pos_out;
+    a.cu_out = cu_seqlens_out;
+    a.src_idx = src_idx;
+    a.total_kept = total_kept;
+    a.nkept = reinterpret_cast<int32_t *>(ws + lay.nkept);
+    a.list = reinterpret_cast<int4 *>(ws + lay.list);
+    a.dst_blk = reinterpret_cast<int32_t *>(ws + lay.dst_blk);
+    a.num_seqs = num_seqs;
+    a.G = G;
+    a.hidden = hidden;
+    a.vec_per_row = (int64_t)hidden * 2 / 16;
+    int rpi = (int)(32768 / ((int64_t)hidden * 2));
+    if (rpi < 1) rpi = 1;
+    if (rpi > G) rpi = G;
+    a.rows_per_item = rpi;
+    a.items_per_block = (G + rpi - 1) / rpi;
+    if (up::launch_compact(a, ds->sms, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return UP_ERR_CUDA;
+    return UP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+// common.cuh -- internal types shared by the kernels of the UniPrefill hot path.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace up {
+
+// Per-sequence work description, written on the device by the plan kernel from
+// cu_seqlens, so the host never needs the sequence lengths.
+struct SeqInfo {
+    int32_t tok_off;   // cu_seqlens[s]
+    int32_t L;         // tokens in the sequence
+    int32_t ns;        // min(n, L): scored queries
+    int32_t q_off;     // first row of q_last for this sequence
+    int32_t nb;        // ceil(L / G)
+    int32_t blk_off;   // cu_blocks[s]
+    int32_t nchunks;   // ceil(L / C): key chunks
+    int32_t mtiles;    // ceil(g * ns / 128): 128-row tiles per KV head
+    int32_t R;         // Hq * ns: softmax rows of the sequence
+    int32_t unit_off;  // first score work unit of the sequence
+    int64_t row_off;   // first global row (exclusive prefix of R)
+    int64_t part_off;  // first float of the (block, row) partial sums
+    int64_t stat_off;  // first float of the (chunk, row) statistics
+};
+static_assert(sizeof(SeqInfo) == 64, "SeqInfo is 64 bytes");
+
+// Device counters at the head of the score workspace.
+struct Counters {
+    int32_t units;       // score work units
+    int32_t blocks;      // sum nb_s
+    int64_t rows;        // sum R_s
+    int32_t pad[12];
+};
+static_assert(sizeof(Counters) == 64, "Counters is 64 bytes");
+
+constexpr int kRowsPerTile = 128;   // rows of one M tile (TMEM lanes)
+constexpr int kChunkQuantum = 256;  // key chunks are multiples of this (and of G)
+
+// Score workspace layout (offsets in bytes, every region 256-byte aligned).
+struct ScoreLayout {
+    size_t seqs, counters, part, mref, lsum, w, total;
+    int64_t max_part, max_stat, max_rows, max_units, max_blocks;
+    int chunk;  // C: keys per work unit
+};
+
+// Everything the scoring kernels read.
+struct ScoreParams {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k;
+    const SeqInfo *seqs;
+    const Counters *counters;
+    float *part;   // [b][r] per sequence: block partial sums (relative to mref)
+    float *mref;   // [c][r] per sequence: reference (log2 units) of the chunk's partials
+    float *lsum;   // [c][r] per sequence: sum of the chunk's partials
+    float *w;      // [c][r] per sequence: final weight of the chunk's partials
+    float *scores;
+    int num_seqs, Hq, Hk, g, d, n, G, C;
+    float scale_log2;  // log2(e) / sqrt(d)
+    unsigned int *err;
+};
+
+__device__ __forceinline__ int find_seq_by_unit(const SeqInfo *seqs, int B, int u) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (seqs[mid].unit_off <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Host-side launchers (each returns the launch's cudaError_t).
+cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, const ScoreParams &p,
+                              int64_t total_tokens, cudaStream_t st);
+cudaError_t launch_score_main(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
+                              cudaStream_t st);
+cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, cudaStream_t st);
+cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const int32_t *cu_seqlens,
+                          int num_seqs, int G, double p, uint8_t *keep, int32_t *kept_tokens,
+                          unsigned int *err, cudaStream_t st);
+
+struct CompactArgs {
+    const uint4 *x;
+    const int32_t *pos;
+    const int32_t *cu_seqlens;
+    const uint8_t *keep;
+    const int32_t *cu_blocks;
+    uint4 *x_out;
+    int32_t *pos_out;
+    int32_t *cu_out;
+    int32_t *src_idx;
+    int32_t *total_kept;
+    int4 *list;        // workspace: kept blocks (src row, dst row, rows, -)
+    int32_t *nkept;    // workspace: number of kept blocks
+    int32_t *dst_blk;  // workspace: destination row of every block
+    int num_seqs, G, hidden, rows_per_item, items_per_block;
+    int64_t vec_per_row;  // hidden * 2 / 16
+};
+cudaError_t launch_compact(const CompactArgs &a, int num_sms, cudaStream_t st);
+
+}  // namespace up

@@ -1,0 +1,131 @@
+// score_simt.cu -- CUDA-core scoring kernel (correctness scaffold for the
+// tensor-core kernel; same work units and the same partial-sum format).
+//
+// One CTA per work unit (sequence s, KV head j, 128-row tile mt, key chunk c);
+// thread = softmax row r = (query head h in group j, query t).  Logits are
+// computed twice: the first pass finds the chunk maximum m of each row (log2
+// units), the second sums 2^(z*log2e/sqrt(d) - m) over every block of the chunk.
+// Source: UniPrefill overview, block-wise importance estimation paragraph.
+#include "common.cuh"
+
+namespace up {
+
+namespace {
+
+constexpr int kKeyTile = 32;
+
+template <int D>
+__device__ __forceinline__ void tile_logits(const __nv_bfloat16 *qT, const float *ks, int tid,
+                                            float (&acc)[kKeyTile]) {
+#pragma unroll
+    for (int kk = 0; kk < kKeyTile; ++kk) acc[kk] = 0.f;
+    for (int c = 0; c < D; ++c) {
+        const float qv = __bfloat162float(qT[c * kRowsPerTile + tid]);
+#pragma unroll
+        for (int kk = 0; kk < kKeyTile; ++kk) acc[kk] = fmaf(qv, ks[kk * D + c], acc[kk]);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kRowsPerTile)
+score_simt_kernel(ScoreParams p) {
+    const int u = blockIdx.x;
+    if (u >= p.counters->units) return;
+    const int s = find_seq_by_unit(p.seqs, p.num_seqs, u);
+    const SeqInfo sq = p.seqs[s];
+    int loc = u - sq.unit_off;
+    const int mt = loc % sq.mtiles;
+    loc /= sq.mtiles;
+    const int c = loc % sq.nchunks;
+    const int j = loc / sq.nchunks;
+
+    extern __shared__ __align__(16) unsigned char smem[];
+    __nv_bfloat16 *qT = reinterpret_cast<__nv_bfloat16 *>(smem);                 // [D][128]
+    float *ks = reinterpret_cast<float *>(smem + D * kRowsPerTile * 2);          // [32][D]
+
+    const int tid = threadIdx.x;
+    const int grows = p.g * sq.ns;  // rows of this KV head group
+    const int rl = mt * kRowsPerTile + tid;
+    const bool valid = rl < grows;
+    const int t = valid ? rl % sq.ns : 0;
+    const int a = sq.L - sq.ns + t;  // absolute position of the query (causal limit)
+    const int64_t r = (int64_t)j * grows + rl;  // row within the sequence: h*ns + t
+
+    for (int idx = tid; idx < kRowsPerTile * D; idx += kRowsPerTile) {
+        const int row = idx / D, cc = idx % D;
+        const int rr = mt * kRowsPerTile + row;
+        __nv_bfloat16 v = __float2bfloat16(0.f);
+        if (rr < grows) {
+            const int hh = rr / sq.ns, tt = rr % sq.ns;
+            v = p.q[((int64_t)(sq.q_off + tt) * p.Hq + j * p.g + hh) * D + cc];
+        }
+        qT[cc * kRowsPerTile + row] = v;
+    }
+
+    const int k0 = c * p.C;
+    const int k1 = min(k0 + p.C, sq.L);
+    float m = -INFINITY;
+    float acc[kKeyTile];
+    for (int pass = 0; pass < 2; ++pass) {
+        float bsum = 0.f, lsum = 0.f;
+        for (int kt = k0; kt < k1; kt += kKeyTile) {
+            __syncthreads();
+            for (int idx = tid; idx < kKeyTile * D; idx += kRowsPerTile) {
+                const int key = kt + idx / D;
+                ks[idx] = key < k1 ? __bfloat162float(
+                                         p.k[((int64_t)(sq.tok_off + key) * p.Hk + j) * D + idx % D])
+                                   : 0.f;
+            }
+            __syncthreads();
+            tile_logits<D>(qT, ks, tid, acc);
+#pragma unroll
+            for (int kk = 0; kk < kKeyTile; ++kk) {
+                const int key = kt + kk;
+                if (key >= k1) break;
+                const bool vis = key <= a;
+                const float z = acc[kk] * p.scale_log2;
+                if (pass == 0) {
+                    if (vis) m = fmaxf(m, z);
+                } else {
+                    const float e = (vis && m != -INFINITY) ? exp2f(z - m) : 0.f;
+                    bsum += e;
+                    if ((key + 1) % p.G == 0 || key + 1 == k1) {
+                        if (valid) p.part[sq.part_off + (int64_t)(key / p.G) * sq.R + r] = bsum;
+                        lsum += bsum;
+                        bsum = 0.f;
+                    }
+                }
+            }
+        }
+        if (pass == 1 && valid) {
+            p.mref[sq.stat_off + (int64_t)c * sq.R + r] = m;
+            p.lsum[sq.stat_off + (int64_t)c * sq.R + r] = lsum;
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const ScoreParams &p, const ScoreLayout &lay, cudaStream_t st) {
+    const size_t smem = (size_t)D * kRowsPerTile * 2 + (size_t)kKeyTile * D * 4;
+    cudaError_t e = cudaFuncSetAttribute(score_simt_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (lay.max_units <= 0) return cudaSuccess;
+    score_simt_kernel<D><<<(unsigned)lay.max_units, kRowsPerTile, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_score_main(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
+                              cudaStream_t st) {
+    (void)num_sms;
+    switch (p.d) {
+        case 64: return launch_d<64>(p, lay, st);
+        case 128: return launch_d<128>(p, lay, st);
+        case 256: return launch_d<256>(p, lay, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace up

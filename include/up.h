@@ -1,0 +1,175 @@
+/*
+ * up.h -- C ABI of the UniPrefill block-sparsification hot path for GB300 (sm_103a).
+ *
+ * UniPrefill drops unimportant tokens during long-context prefill.  At one
+ * full-attention layer the last n queries of each sequence score fixed blocks
+ * of G key tokens; the highest-scoring blocks are kept until their cumulative
+ * score reaches p; the hidden states and position ids of the kept tokens are
+ * gathered into a compacted batch that every later layer consumes.
+ *
+ * Sources: "UniPrefill: 블록 단위 동적 희소화를 통한 범용적 롱 컨텍스트 프리필 가속화"
+ * (aitrends.kr overview; paragraphs on block-wise importance estimation, top-p
+ * selection, system integration and sparsity propagation) and the UniPrefill
+ * abstract (chatpaper.ai; continuous-batching operator).
+ *
+ * Conventions shared by every call
+ *   - All pointers are DEVICE pointers unless stated otherwise.  The caller
+ *     allocates and owns every buffer, including the workspace.  The library
+ *     never allocates, frees or synchronises; every call is asynchronous and
+ *     ordered on `stream`.
+ *   - Sequences are continuously batched (varlen): `cu_seqlens` is int32
+ *     [num_seqs + 1], cu_seqlens[0] = 0, non-decreasing, and
+ *     cu_seqlens[num_seqs] = total_tokens.  L_s = cu_seqlens[s+1] - cu_seqlens[s].
+ *   - Tensors are token-major, row-major and contiguous; "bf16" buffers hold
+ *     IEEE bfloat16 values.
+ *   - nb_s = ceil(L_s / G) blocks per sequence; cu_blocks is int32
+ *     [num_seqs + 1], the exclusive prefix sum of nb_s.
+ *   - Host-checkable arguments are validated before any launch; a rejected
+ *     call launches nothing and returns the error.  Errors found on the device
+ *     (a malformed cu_seqlens, a sequence beyond a kernel's size limit, an
+ *     expired bounded wait) set a sticky device error word that
+ *     up_get_device_error() reports; the affected outputs are then unspecified.
+ *   - Functions are thread-safe; the first call on a device queries its
+ *     attributes and sets kernel attributes for it.
+ */
+#ifndef UP_H_
+#define UP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *up_stream_t;
+
+typedef enum {
+    UP_OK = 0,
+    UP_ERR_INVALID_ARG = 1,  /* null pointer, bad size, p out of range, misaligned buffer */
+    UP_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement (head_dim, G, ...) */
+    UP_ERR_WORKSPACE = 3,    /* workspace pointer null or smaller than the *_workspace() size */
+    UP_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
+    UP_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired (reported by up_get_device_error) */
+    UP_ERR_DEVICE = 6        /* a device-side argument check failed (reported by up_get_device_error) */
+} up_status;
+
+/* Device error bits reported by up_get_device_error(). */
+#define UP_DEVERR_BAD_CU_SEQLENS 0x1u  /* cu_seqlens[0] != 0, decreasing, or last != total_tokens */
+#define UP_DEVERR_SELECT_TOO_MANY_BLOCKS 0x2u /* a sequence has more than UP_SELECT_MAX_BLOCKS blocks */
+#define UP_DEVERR_TIMEOUT 0x4u         /* a bounded wait inside a kernel gave up */
+
+/* Largest nb_s that up_select_topp sorts on chip (1M tokens at G = 64). */
+#define UP_SELECT_MAX_BLOCKS 16384
+
+/* Static text for a status code. */
+const char *up_status_string(up_status status);
+
+/*
+ * Block scoring.
+ *
+ * Source: UniPrefill overview, block-wise importance estimation paragraph (the
+ * last n queries are dotted with all keys; block scores come from softmax
+ * attention mass) and drop-criterion paragraph (tokens whose softmax
+ * probability is near zero are dropped).
+ *
+ * For sequence s let n_s = min(n, L_s).  Query t in [0, n_s) sits at absolute
+ * position a_t = L_s - n_s + t and sees keys i <= a_t (causal).  For query head
+ * h (KV head j = h / (Hq/Hk)):
+ *     P[h,t,i] = softmax_i( q[t,h,:] . k[i,j,:] / sqrt(d) )   over i <= a_t
+ *     scores[cu_blocks[s] + b] = (1 / (n_s*Hq)) * sum_{h,t} sum_{i in block b} P[h,t,i]
+ * so each sequence's scores sum to 1.  Block b covers tokens [bG, min((b+1)G, L_s)).
+ *
+ *   q_last     bf16 [sum_s n_s, Hq, d]: the last n_s query rows of every
+ *              sequence, packed in sequence order (RoPE already applied).
+ *   k          bf16 [total_tokens, Hk, d] keys (RoPE already applied).
+ *   cu_seqlens int32 [num_seqs+1].
+ *   Hq, Hk     query / KV heads, Hq % Hk == 0, Hq/Hk <= 16.
+ *   d          head_dim: 64, 128 or 256.
+ *   n          observation window (last queries), 1 <= n <= 1024.
+ *   G          block size: 16, 32, 64, 128 or 256.
+ *   scores     fp32 [sum_s nb_s] (output).  Capacity needed: at most
+ *              total_tokens/G + num_seqs entries.
+ *   cu_blocks  int32 [num_seqs+1] (output).
+ *   workspace  device scratch of at least up_score_blocks_workspace(...) bytes,
+ *              256-byte aligned; its contents on entry do not matter.
+ * Scores are deterministic: a repeat call on the same inputs returns the same bits.
+ */
+size_t up_score_blocks_workspace(int num_seqs, int64_t total_tokens, int Hq, int Hk, int d,
+                                 int n, int G);
+
+up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_seqlens,
+                          int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
+                          int G, float *scores, int32_t *cu_blocks, void *workspace,
+                          size_t workspace_bytes, up_stream_t stream);
+
+/*
+ * Top-p block selection.
+ *
+ * Source: UniPrefill overview, top-p selection paragraph: blocks sorted by
+ * score are kept until their cumulative sum reaches p (e.g. 0.99).
+ *
+ * Per sequence, blocks are ranked by (score descending, block index
+ * ascending); the cumulative score is taken in fp64 in rank order; the kept
+ * set is the shortest prefix whose cumulative score is >= p, crossing block
+ * included.  p >= 1 keeps every block; if rounding leaves the total below p,
+ * every block is kept.
+ *
+ *   scores, cu_blocks  as produced by up_score_blocks (scores >= 0).
+ *   cu_seqlens         int32 [num_seqs+1] (block lengths for kept_tokens).
+ *   p                  0 < p; p >= 1 keeps all.
+ *   keep               uint8 [sum nb_s] (output): 1 kept, 0 dropped, original order.
+ *   kept_tokens        int32 [num_seqs] (output): tokens in the kept blocks.
+ * Sequences with nb_s > UP_SELECT_MAX_BLOCKS raise UP_DEVERR_SELECT_TOO_MANY_BLOCKS.
+ */
+up_status up_select_topp(const float *scores, const int32_t *cu_blocks,
+                         const int32_t *cu_seqlens, int num_seqs, int G, double p,
+                         uint8_t *keep, int32_t *kept_tokens, up_stream_t stream);
+
+/*
+ * Compaction (sparsity propagation).
+ *
+ * Source: UniPrefill overview, sparsity-propagation paragraph (every later
+ * sub-layer takes only the kept tokens) and system-integration paragraph (the
+ * positions of dropped/kept tokens travel with the batch so decode addresses
+ * the right KV-cache slots).
+ *
+ * For each sequence in order and each kept block in ascending order, the
+ * block's rows of x and pos are appended to x_out / pos_out.  Positions are
+ * gathered, not renumbered.
+ *
+ *   x               bf16 [total_tokens, hidden], 16-byte aligned; hidden % 8 == 0.
+ *   pos             int32 [total_tokens].
+ *   keep, cu_blocks as produced above.
+ *   x_out           bf16 [capacity, hidden], 16-byte aligned; capacity must be
+ *                   >= the number of kept tokens (total_tokens is always enough).
+ *   pos_out         int32 [capacity].
+ *   cu_seqlens_out  int32 [num_seqs+1] (output): cu_seqlens of the compacted batch.
+ *   src_idx         int32 [capacity] or NULL: source row of every output row.
+ *   total_kept      int32 [1] (output): number of kept rows (= cu_seqlens_out[num_seqs]).
+ *   workspace       at least up_compact_workspace(...) bytes, 256-byte aligned.
+ * The output size lives on the device; reading it on the host is the caller's
+ * choice (one device-to-host copy of total_kept).
+ */
+size_t up_compact_workspace(int num_seqs, int64_t total_tokens, int G);
+
+up_status up_compact(const void *x, const int32_t *pos, int hidden, const int32_t *cu_seqlens,
+                     int num_seqs, int64_t total_tokens, int G, const uint8_t *keep,
+                     const int32_t *cu_blocks, void *x_out, int32_t *pos_out,
+                     int32_t *cu_seqlens_out, int32_t *src_idx, int32_t *total_kept,
+                     void *workspace, size_t workspace_bytes, up_stream_t stream);
+
+/*
+ * Reads and clears the sticky device error word of the current device
+ * (UP_DEVERR_* bits; 0 if none).  This call synchronises the device.
+ * Returns UP_OK if no bit was set, UP_ERR_TIMEOUT if the timeout bit was set,
+ * UP_ERR_DEVICE for any other bit, UP_ERR_CUDA if the copy itself failed.
+ */
+up_status up_get_device_error(uint32_t *bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UP_H_ */

@@ -1,0 +1,110 @@
+"""The C-ABI library builds, loads without a GPU, exports what include/up.h
+declares, and rejects bad host-side arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_long_up_gb300 as up
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    up.build()
+    return up.lib()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(up_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert {"up_score_blocks", "up_select_topp", "up_compact"} <= names
+    for name in sorted(names):
+        assert hasattr(L, name), f"{name} is declared in include/ but not exported"
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert L.up_status_string(code)
+    assert L.up_status_string(0) == b"ok"
+
+
+def test_workspace_sizes(L):
+    # the Llama-3.1-8B layer at 128K: partial sums of 4096 rows x 2048 blocks dominate
+    ws = up.score_blocks_workspace(1, 131072, 32, 8, 128, 128, 64)
+    assert 4096 * 2049 * 4 <= ws < 64 << 20
+    assert up.score_blocks_workspace(1, 4096, 8, 2, 64, 128, 64) > 0
+    # unsupported shapes report 0
+    assert up.score_blocks_workspace(1, 4096, 8, 3, 64, 128, 64) == 0
+    assert up.score_blocks_workspace(1, 4096, 8, 2, 96, 128, 64) == 0
+    assert up.score_blocks_workspace(1, 4096, 8, 2, 64, 128, 48) == 0
+    assert up.compact_workspace(8, 401408, 64) >= (401408 // 64 + 8) * 20
+    assert up.compact_workspace(1, 100, 7) == 0
+
+
+P = ctypes.c_void_p
+
+
+def _fake(addr=256):
+    return ctypes.c_void_p(addr)
+
+
+def test_score_rejects_bad_arguments(L):
+    args = dict(q=_fake(), k=_fake(), cu=_fake(), B=1, T=4096, Hq=8, Hk=2, d=64, n=128, G=64,
+                sc=_fake(), cb=_fake(), ws=_fake(), wsb=1 << 30)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return L.up_score_blocks(a["q"], a["k"], a["cu"], a["B"], a["T"], a["Hq"], a["Hk"],
+                                 a["d"], a["n"], a["G"], a["sc"], a["cb"], a["ws"], a["wsb"], None)
+
+    assert call(Hk=3) == 1          # Hq % Hk
+    assert call(n=0) == 1
+    assert call(B=-1) == 1
+    assert call(cu=None) == 1
+    assert call(q=None) == 1
+    assert call(q=_fake(258)) == 1  # q_last not 16-byte aligned
+    assert call(d=96) == 2
+    assert call(G=48) == 2
+    assert call(n=2048) == 2
+    assert call(Hq=64, Hk=2) == 2   # group of 32 query heads per KV head
+    assert call(ws=None) == 3
+    assert call(wsb=1024) == 3
+    assert call(ws=_fake(272)) == 3  # workspace not 256-byte aligned
+
+
+def test_select_and_compact_reject_bad_arguments(L):
+    assert L.up_select_topp(_fake(), _fake(), _fake(), 1, 64, 0.0, _fake(), _fake(), None) == 1
+    assert L.up_select_topp(_fake(), _fake(), _fake(), 1, 64, float("nan"), _fake(), _fake(), None) == 1
+    assert L.up_select_topp(_fake(), _fake(), _fake(), 1, 40, 0.9, _fake(), _fake(), None) == 2
+    assert L.up_select_topp(None, _fake(), _fake(), 1, 64, 0.9, _fake(), _fake(), None) == 1
+
+    def comp(hidden=512, x=_fake(), xo=_fake(), ws=_fake(), wsb=1 << 30, G=64, tk=_fake()):
+        return L.up_compact(x, _fake(), hidden, _fake(), 1, 4096, G, _fake(), _fake(), xo,
+                            _fake(), _fake(), None, tk, ws, wsb, None)
+
+    assert comp(hidden=500) == 2
+    assert comp(G=65) == 2
+    assert comp(x=_fake(264)) == 1
+    assert comp(xo=_fake(264)) == 1
+    assert comp(tk=None) == 1
+    assert comp(ws=None) == 3
+    assert comp(wsb=16) == 3
+
+
+def test_python_binding_fails_loudly_without_cuda_tensors(L):
+    import torch
+    q = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        up.score_blocks(q, q, torch.zeros(2, dtype=torch.int32), 4, 64)

@@ -1,0 +1,206 @@
+"""GPU parity: the C-ABI CUDA path against the fp64 oracle on the same seeded inputs."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_long_up_gb300 as up
+import oracle
+from block_sparse_long_up_gb300 import synth
+
+from parity_util import (full_check, gpu_compact, gpu_scores, gpu_select, keep_mismatch,
+                         score_failures, to_dev_bf16, to_dev_i32)
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    up.build()
+    up.lib()
+    yield
+    assert up.get_device_error() == 0
+
+
+@pytest.mark.parametrize("lens,Hq,Hk,d,n,G,p,gain", [
+    ([300], 4, 1, 64, 16, 16, 0.9, 5.0),
+    ([1000, 37, 513], 8, 2, 128, 64, 64, 0.95, 5.0),     # ragged tails, several chunks
+    ([5, 1, 129], 4, 4, 64, 128, 32, 0.99, 5.0),         # L < n, L == 1
+    ([2048], 16, 2, 256, 100, 128, 0.9, 5.0),            # d=256, g=8, 800 rows (ragged tile)
+    ([700, 4096], 32, 8, 128, 128, 256, 0.99, 5.0),
+    ([777], 2, 1, 128, 1, 64, 0.5, 5.0),                 # one query
+    ([3000, 1500], 8, 2, 64, 128, 64, 0.99, None),       # literal unit shift: dense regime
+    ([9000], 12, 4, 128, 48, 16, 0.999, 5.0),            # G=16, many blocks per chunk
+])
+def test_small_shapes(lens, Hq, Hk, d, n, G, p, gain):
+    inp = synth.make_inputs(lens, Hq, Hk, d, n, 0.05, gain=gain, hidden=64, seed=sum(lens) + d)
+    full_check(inp, n, G, p)
+
+
+@pytest.mark.parametrize("gain", [5.0, None])
+def test_gqa8x2_d64_4k_workload(gain):
+    inp = synth.make_workload("gqa8x2_d64_4k", gain=gain)
+    w = synth.WORKLOADS["gqa8x2_d64_4k"]
+    rep = full_check(inp, w["n"], w["G"], w["p"])
+    if gain is not None:
+        assert rep["kept"] < rep["blocks"] // 4
+
+
+def test_scores_are_deterministic():
+    inp = synth.make_inputs([5000, 3000], 8, 2, 128, 128, 0.05, seed=3)
+    a, _ = gpu_scores(inp, 128, 64)
+    b, _ = gpu_scores(inp, 128, 64)
+    assert np.array_equal(a, b)
+
+
+def test_empty_batch_and_empty_sequences():
+    inp = synth.make_inputs([0, 300, 0, 65, 0], 4, 2, 64, 32, 0.05, hidden=16, seed=4)
+    full_check(inp, 32, 64, 0.9)
+    # no sequences at all
+    k = torch.zeros(0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(0, 4, 64, dtype=torch.bfloat16, device="cuda")
+    cu = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sc, cb = up.score_blocks(q, k, cu, 32, 64)
+    keep, kt = up.select_topp(sc, cb, cu, 64, 0.9)
+    x = torch.zeros(0, 16, dtype=torch.bfloat16, device="cuda")
+    pos = torch.zeros(0, dtype=torch.int32, device="cuda")
+    _, _, cuo, tk, _ = up.compact(x, pos, cu, 64, keep, cb)
+    torch.cuda.synchronize()
+    assert cb.cpu().tolist() == [0] and cuo.cpu().tolist() == [0] and tk.item() == 0
+
+
+def test_block_larger_than_sequence_and_p_extremes():
+    inp = synth.make_inputs([100, 40, 256], 4, 1, 64, 16, 0.05, hidden=32, seed=8)
+    full_check(inp, 16, 256, 0.5)           # G >= L: one block per sequence, score 1
+    g_sc, g_cb = gpu_scores(inp, 16, 256)
+    np.testing.assert_allclose(g_sc, 1.0, atol=1e-5)
+    g_sc, g_cb = gpu_scores(inp, 16, 32)
+    keep, kt = gpu_select(g_sc, g_cb, inp.cu_seqlens, 32, 1.0)
+    assert keep.all() and kt.tolist() == [100, 40, 256]
+    keep, kt = gpu_select(g_sc, g_cb, inp.cu_seqlens, 32, 1e-9)
+    for s in range(3):
+        seg = keep[g_cb[s]:g_cb[s + 1]]
+        assert seg.sum() == 1 and np.argmax(seg) == np.argmax(g_sc[g_cb[s]:g_cb[s + 1]])
+
+
+def _golden_topp():
+    out = []
+    with open(os.path.join(GOLDEN, "topp_hand_enumerated.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                p, sc, kept = (x.strip() for x in line.split(";"))
+                out.append((float(p), [float(v) for v in sc.split(",")],
+                            sorted(int(v) for v in kept.split(","))))
+    return out
+
+
+@pytest.mark.parametrize("p,scores,kept", _golden_topp())
+def test_select_hand_enumerated(p, scores, kept):
+    nb, G = len(scores), 16
+    keep, kt = gpu_select(np.array(scores), np.array([0, nb]), np.array([0, nb * G]), G, p)
+    assert sorted(np.nonzero(keep)[0].tolist()) == kept
+    assert kt.tolist() == [len(kept) * G]
+
+
+@pytest.mark.parametrize("nb", [1, 2, 1000, 1024, 1025, 4096, 16384])
+def test_select_ties_and_sizes(nb):
+    """Scores with many exact ties (a few distinct values) and all power-of-two
+    boundaries of the on-chip sort; the oracle's rule on the same fp32 scores."""
+    rng = np.random.default_rng(nb)
+    vals = np.array([1.0, 0.5, 0.25, 0.125], dtype=np.float32)
+    sc = vals[rng.integers(0, 4, size=nb)].astype(np.float64)
+    sc = (sc / sc.sum()).astype(np.float32).astype(np.float64)
+    G = 64
+    cu = np.array([0, nb * G - 5], np.int32)
+    cb = np.array([0, nb], np.int32)
+    for p in (0.1, 0.5, 0.9, 0.999, 1.0):
+        keep, kt = gpu_select(sc, cb, cu, G, p)
+        ok, okt, ci, ce = oracle.select_topp(sc, cb, cu, G, p)
+        hard, _ = keep_mismatch(keep, ok, ci, ce, p)
+        assert hard == 0
+        if np.array_equal(keep, ok):
+            assert kt.tolist() == okt.tolist()
+
+
+def test_select_rejects_too_many_blocks():
+    nb = up.SELECT_MAX_BLOCKS + 1
+    sc = np.full(nb, 1.0 / nb)
+    gpu_select(sc, np.array([0, nb]), np.array([0, nb * 16]), 16, 0.5)
+    assert up.get_device_error() == 0x2
+
+
+@pytest.mark.parametrize("hidden", [8, 520, 4096])
+def test_compact_random_keep(hidden):
+    rng = np.random.default_rng(hidden)
+    lens = [130, 0, 64, 1, 1000, 63]
+    G = 32
+    cu = np.zeros(len(lens) + 1, np.int32)
+    cu[1:] = np.cumsum(lens)
+    nbs = [(L + G - 1) // G for L in lens]
+    cb = np.zeros(len(lens) + 1, np.int32)
+    cb[1:] = np.cumsum(nbs)
+    x = rng.integers(0, 1 << 16, size=(int(cu[-1]), hidden), dtype=np.uint16)
+    pos = rng.integers(-5, 1 << 30, size=int(cu[-1])).astype(np.int32)
+    for prob in (0.0, 0.3, 1.0):
+        keep = (rng.random(int(cb[-1])) < prob).astype(np.uint8)
+        xo, po, cuo, src, T = gpu_compact(x, pos, cu, G, keep, cb)
+        ox, opos, ocu, osrc = oracle.compact(x, pos, cu, G, keep, cb)
+        assert T == len(opos)
+        np.testing.assert_array_equal(cuo, ocu)
+        np.testing.assert_array_equal(src, osrc)
+        np.testing.assert_array_equal(po, opos)
+        assert np.array_equal(xo, ox)
+
+
+def test_bad_cu_seqlens_sets_device_error():
+    k = torch.zeros(100, 1, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(10, 1, 64, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 60, 50], dtype=torch.int32, device="cuda")  # decreasing, wrong total
+    up.score_blocks(q, k, cu, 5, 64)
+    assert up.get_device_error() == 0x1
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads (the shapes the benchmark times)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,gain", [
+    ("llama31_8b_32k", 5.0),
+    ("llama31_8b_128k", 5.0),
+    ("llama31_8b_128k", None),
+    ("llama31_8b_varlen8_392k", 5.0),
+])
+def test_full_size_workloads(name, gain):
+    w = synth.WORKLOADS[name]
+    inp = synth.make_workload(name, gain=gain)
+    rep = full_check(inp, w["n"], w["G"], w["p"])
+    print(name, gain, rep)
+
+
+def test_full_size_d256_sweep():
+    name = "gqa16x2_d256_128k_sweep"
+    w = synth.WORKLOADS[name]
+    sweep = w["sweep"]
+    for n in sweep["n"]:
+        inp = synth.make_workload(name, n=n, with_x=(n == 128))
+        mass = oracle.token_mass(inp.q_last, inp.k, inp.cu_seqlens, inp.Hq, inp.Hk, inp.d, n)
+        for G in sweep["G"]:
+            orc_sc, orc_cb = oracle.block_scores(mass, inp.cu_seqlens, G)
+            g_sc, g_cb = gpu_scores(inp, n, G)
+            np.testing.assert_array_equal(g_cb, orc_cb)
+            nbad, worst = score_failures(g_sc, orc_sc)
+            assert nbad == 0, (n, G, nbad, worst)
+            for p in sweep["p"]:
+                ok, _, ci, ce = oracle.select_topp(orc_sc, orc_cb, inp.cu_seqlens, G, p)
+                gk, _ = gpu_select(g_sc, g_cb, inp.cu_seqlens, G, p)
+                hard, excused = keep_mismatch(gk, ok, ci, ce, p)
+                assert hard == 0, (n, G, p, hard)
+                if n == 128 and G == 64:
+                    xo, po, cuo, src, T = gpu_compact(inp.x, inp.pos, inp.cu_seqlens, G, gk, g_cb)
+                    ox, opos, ocu, osrc = oracle.compact(inp.x, inp.pos, inp.cu_seqlens, G, gk, g_cb)
+                    assert np.array_equal(xo, ox) and np.array_equal(src, osrc)
+                    np.testing.assert_array_equal(cuo, ocu)
