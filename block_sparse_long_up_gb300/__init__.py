@@ -20,7 +20,7 @@ import torch
 from . import _build
 
 __all__ = ["build", "lib", "UpError", "score_blocks_workspace", "score_blocks", "select_topp",
-           "compact_workspace", "compact", "get_device_error", "Sparsifier", "SELECT_MAX_BLOCKS"]
+           "compact_workspace", "compact", "compact_noalloc", "get_device_error", "Sparsifier", "SELECT_MAX_BLOCKS"]
 
 SELECT_MAX_BLOCKS = 16384
 _lib = None
@@ -59,6 +59,8 @@ def lib():
     L.up_compact_workspace.restype = SZ
     L.up_compact.argtypes = [P, P, I, P, I, I64, I, P, P, P, P, P, P, P, P, SZ, P]
     L.up_compact.restype = I
+    L.up_compact_noalloc.argtypes = [P, P, I, P, I, I64, I, P, P, P, P, P, P, P, P]
+    L.up_compact_noalloc.restype = I
     L.up_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.up_get_device_error.restype = I
     _lib = L
@@ -186,6 +188,23 @@ def compact(x, pos, cu_seqlens, G, keep, cu_blocks, x_out=None, pos_out=None,
                           _ptr(src_idx), _ptr(total_kept), _ptr(workspace),
                           workspace.numel() * workspace.element_size(), _stream(stream))
     _check("up_compact", st)
+    return x_out, pos_out, cu_seqlens_out, total_kept, src_idx
+
+
+def compact_noalloc(x, pos, cu_seqlens, G, keep, cu_blocks, x_out, pos_out, cu_seqlens_out,
+                    src_idx, total_kept, stream=None):
+    """up_compact without a workspace, for callers that cannot allocate device
+    memory: every output buffer must be passed in, and the library's fixed
+    scratch is used instead (see up_compact_noalloc in include/up.h)."""
+    for t, name in ((x, "x"), (x_out, "x_out")):
+        _need(t, name, torch.bfloat16)
+    total, hidden = x.shape
+    B = cu_seqlens.numel() - 1
+    st = lib().up_compact_noalloc(_ptr(x), _ptr(pos), hidden, _ptr(cu_seqlens), B, total, G,
+                                  _ptr(keep), _ptr(cu_blocks), _ptr(x_out), _ptr(pos_out),
+                                  _ptr(cu_seqlens_out), _ptr(src_idx), _ptr(total_kept),
+                                  _stream(stream))
+    _check("up_compact_noalloc", st)
     return x_out, pos_out, cu_seqlens_out, total_kept, src_idx
 
 

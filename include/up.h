@@ -161,6 +161,38 @@ up_status up_compact(const void *x, const int32_t *pos, int hidden, const int32_
                      void *workspace, size_t workspace_bytes, up_stream_t stream);
 
 /*
+ * Compaction without a caller-supplied workspace.
+ *
+ * The UniPrefill pages have no counterpart of this entry point; it exists for
+ * callers that cannot allocate device memory when they compact -- an engine
+ * that has reserved nearly all HBM for its KV cache, or a serving loop that
+ * must not call cudaMalloc because it can synchronise the device.
+ *
+ * It computes exactly what up_compact computes, with the same arguments minus
+ * the workspace.  Its scratch (kept-block list, per-block destination rows and
+ * a counter, about 1.3 MB) is a fixed array inside the library that every GPU
+ * loading the library holds until the process exits; the call itself
+ * allocates and frees nothing.
+ *   - Limit: total_tokens / G + num_seqs <= UP_COMPACT_NOALLOC_MAX_BLOCKS
+ *     (4M tokens at G = 64); larger batches return UP_ERR_WORKSPACE and launch
+ *     nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array.  Each call rewrites every
+ *     scratch entry it reads, so no clearing is needed, but calls that overlap
+ *     on the GPU (different streams, no ordering between them) race on it and
+ *     give wrong results.
+ */
+#define UP_COMPACT_NOALLOC_MAX_BLOCKS 65536
+
+up_status up_compact_noalloc(const void *x, const int32_t *pos, int hidden,
+                             const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int G,
+                             const uint8_t *keep, const int32_t *cu_blocks, void *x_out,
+                             int32_t *pos_out, int32_t *cu_seqlens_out, int32_t *src_idx,
+                             int32_t *total_kept, up_stream_t stream);
+
+/*
  * Reads and clears the sticky device error word of the current device
  * (UP_DEVERR_* bits; 0 if none).  This call synchronises the device.
  * Returns UP_OK if no bit was set, UP_ERR_TIMEOUT if the timeout bit was set,
