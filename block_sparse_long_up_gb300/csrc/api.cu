@@ -59,6 +59,7 @@ int choose_chunk(int B, int64_t total, int Hq, int Hk, int n) {
 up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int n, int G) {
     up::ScoreLayout L{};
     const int g = Hq / Hk;
+    L.total_tokens = total;
     L.chunk = choose_chunk(B, total, Hq, Hk, n);
     const int64_t nn = n < total ? n : total;
     const int64_t ns_sum = ((int64_t)n * B < total) ? (int64_t)n * B : total;
@@ -66,7 +67,7 @@ up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int n, int G)
     L.max_rows = (int64_t)Hq * ns_sum;
     L.max_part = (int64_t)Hq * nn * L.max_blocks;
     const int64_t max_chunks = total / L.chunk + B;
-    L.max_stat = (int64_t)Hq * nn * max_chunks;
+    L.max_stat = (int64_t)Hq * nn * max_chunks * up::kSlotsPerChunk;
     L.max_units = (int64_t)Hk * ((g * nn + up::kRowsPerTile - 1) / up::kRowsPerTile) * max_chunks;
     size_t off = 0;
     L.seqs = off;     off = align256(off + sizeof(up::SeqInfo) * (size_t)(B > 0 ? B : 1));
@@ -75,6 +76,7 @@ up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int n, int G)
     L.mref = off;     off = align256(off + sizeof(float) * (size_t)L.max_stat);
     L.lsum = off;     off = align256(off + sizeof(float) * (size_t)L.max_stat);
     L.w = off;        off = align256(off + sizeof(float) * (size_t)L.max_stat);
+    L.flags = off;    off = align256(off + sizeof(int32_t) * (size_t)(16 * L.max_units + 16));
     L.total = off;
     return L;
 }
@@ -180,6 +182,9 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     p.lsum = reinterpret_cast<float *>(ws + lay.lsum);
     p.w = reinterpret_cast<float *>(ws + lay.w);
     p.scores = scores;
+    p.flag_list = reinterpret_cast<int32_t *>(ws + lay.flags);
+    p.max_units = (int)lay.max_units;
+    p.flag_cap = (int)(16 * lay.max_units + 16);
     p.num_seqs = num_seqs;
     p.Hq = Hq; p.Hk = Hk; p.g = Hq / Hk; p.d = d; p.n = n; p.G = G; p.C = lay.chunk;
     p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
@@ -188,6 +193,7 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
         return UP_ERR_CUDA;
     if (num_seqs == 0 || total_tokens == 0) return UP_OK;
     if (up::launch_score_main(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
+    if (up::launch_score_fallback(p, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_finalize(p, lay, s) != cudaSuccess) return UP_ERR_CUDA;
     return UP_OK;
 }

@@ -31,17 +31,28 @@ struct Counters {
     int32_t units;       // score work units
     int32_t blocks;      // sum nb_s
     int64_t rows;        // sum R_s
-    int32_t pad[12];
+    int32_t flagged;     // units queued for the exact fallback
+    int32_t pad[11];
 };
 static_assert(sizeof(Counters) == 64, "Counters is 64 bytes");
 
 constexpr int kRowsPerTile = 128;   // rows of one M tile (TMEM lanes)
+constexpr int kTileKeys = 256;      // keys of one MMA tile (N)
 constexpr int kChunkQuantum = 256;  // key chunks are multiples of this (and of G)
+// Statistics slots per key chunk: the tiles of a chunk alternate between two
+// softmax warpgroups, and each keeps its own reference, so slot = tile parity.
+constexpr int kSlotsPerChunk = 2;
+
+// Statistics slot of block b (G divides kTileKeys, C is a multiple of it).
+__host__ __device__ __forceinline__ int block_slot(int b, int G, int C) {
+    const int key = b * G;
+    return kSlotsPerChunk * (key / C) + ((key % C) / kTileKeys) % kSlotsPerChunk;
+}
 
 // Score workspace layout (offsets in bytes, every region 256-byte aligned).
 struct ScoreLayout {
-    size_t seqs, counters, part, mref, lsum, w, total;
-    int64_t max_part, max_stat, max_rows, max_units, max_blocks;
+    size_t seqs, counters, part, mref, lsum, w, flags, total;
+    int64_t max_part, max_stat, max_rows, max_units, max_blocks, total_tokens;
     int chunk;  // C: keys per work unit
 };
 
@@ -56,6 +67,9 @@ struct ScoreParams {
     float *lsum;   // [c][r] per sequence: sum of the chunk's partials
     float *w;      // [c][r] per sequence: final weight of the chunk's partials
     float *scores;
+    int32_t *flag_list;  // units whose softmax sums overflowed (exact fallback)
+    int max_units;
+    int flag_cap;        // capacity of flag_list
     int num_seqs, Hq, Hk, g, d, n, G, C;
     float scale_log2;  // log2(e) / sqrt(d)
     unsigned int *err;
@@ -75,6 +89,7 @@ cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, con
                               int64_t total_tokens, cudaStream_t st);
 cudaError_t launch_score_main(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
                               cudaStream_t st);
+cudaError_t launch_score_fallback(const ScoreParams &p, int num_sms, cudaStream_t st);
 cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, cudaStream_t st);
 cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const int32_t *cu_seqlens,
                           int num_seqs, int G, double p, uint8_t *keep, int32_t *kept_tokens,

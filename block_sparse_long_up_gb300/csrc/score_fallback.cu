@@ -1,0 +1,140 @@
+// score_simt.cu -- exact CUDA-core fallback for score work units.
+//
+// The tensor-core kernel measures every partial sum against a reference taken
+// from the first key tile its warpgroup sees in a work unit.  If a later tile of
+// the same unit holds logits more than ~115 binary orders of magnitude above
+// that reference, its fp32 sums overflow; the kernel then queues the unit here.
+// This kernel recomputes such a unit with two passes over the logits: the first
+// finds each row's exact maximum m over the unit's keys (log2 units), the
+// second sums 2^(z*log2e/sqrt(d) - m) over every block.  Both statistics slots
+// of the chunk get the same reference m; each gets the sum of the blocks of its
+// key tiles (even / odd tiles of the chunk).  The queue is empty for ordinary
+// attention logits.
+// Source: UniPrefill overview, block-wise importance estimation paragraph.
+#include "common.cuh"
+
+namespace up {
+
+namespace {
+
+constexpr int kKeyTile = 32;
+
+template <int D>
+__device__ __forceinline__ void tile_logits(const __nv_bfloat16 *qT, const float *ks, int tid,
+                                            float (&acc)[kKeyTile]) {
+#pragma unroll
+    for (int kk = 0; kk < kKeyTile; ++kk) acc[kk] = 0.f;
+    for (int c = 0; c < D; ++c) {
+        const float qv = __bfloat162float(qT[c * kRowsPerTile + tid]);
+#pragma unroll
+        for (int kk = 0; kk < kKeyTile; ++kk) acc[kk] = fmaf(qv, ks[kk * D + c], acc[kk]);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kRowsPerTile)
+score_fallback_kernel(ScoreParams p) {
+    const int nflag = min(p.counters->flagged, p.flag_cap);
+    extern __shared__ __align__(16) unsigned char smem[];
+    __nv_bfloat16 *qT = reinterpret_cast<__nv_bfloat16 *>(smem);                 // [D][128]
+    float *ks = reinterpret_cast<float *>(smem + D * kRowsPerTile * 2);          // [32][D]
+    const int tid = threadIdx.x;
+    for (int fi = blockIdx.x; fi < nflag; fi += gridDim.x) {
+        const int u = p.flag_list[fi];
+        const int s = find_seq_by_unit(p.seqs, p.num_seqs, u);
+        const SeqInfo sq = p.seqs[s];
+        int loc = u - sq.unit_off;
+        const int mt = loc % sq.mtiles;
+        loc /= sq.mtiles;
+        const int c = loc % sq.nchunks;
+        const int j = loc / sq.nchunks;
+
+        const int grows = p.g * sq.ns;
+        const int rl = mt * kRowsPerTile + tid;
+        const bool valid = rl < grows;
+        const int t = valid ? rl % sq.ns : 0;
+        const int a = sq.L - sq.ns + t;
+        const int64_t r = (int64_t)j * grows + rl;
+
+        __syncthreads();
+        for (int idx = tid; idx < kRowsPerTile * D; idx += kRowsPerTile) {
+            const int row = idx / D, cc = idx % D;
+            const int rr = mt * kRowsPerTile + row;
+            __nv_bfloat16 v = __float2bfloat16(0.f);
+            if (rr < grows) {
+                const int hh = rr / sq.ns, tt = rr % sq.ns;
+                v = p.q[((int64_t)(sq.q_off + tt) * p.Hq + j * p.g + hh) * D + cc];
+            }
+            qT[cc * kRowsPerTile + row] = v;
+        }
+
+        const int k0 = c * p.C;
+        const int k1 = min(k0 + p.C, sq.L);
+        float m = -INFINITY;
+        float acc[kKeyTile];
+        float lsum[kSlotsPerChunk] = {0.f, 0.f};
+        for (int pass = 0; pass < 2; ++pass) {
+            float bsum = 0.f;
+            for (int kt = k0; kt < k1; kt += kKeyTile) {
+                __syncthreads();
+                for (int idx = tid; idx < kKeyTile * D; idx += kRowsPerTile) {
+                    const int key = kt + idx / D;
+                    ks[idx] = key < k1 ? __bfloat162float(
+                                             p.k[((int64_t)(sq.tok_off + key) * p.Hk + j) * D + idx % D])
+                                       : 0.f;
+                }
+                __syncthreads();
+                tile_logits<D>(qT, ks, tid, acc);
+#pragma unroll
+                for (int kk = 0; kk < kKeyTile; ++kk) {
+                    const int key = kt + kk;
+                    if (key >= k1) break;
+                    const bool vis = key <= a;
+                    const float z = acc[kk] * p.scale_log2;
+                    if (pass == 0) {
+                        if (vis) m = fmaxf(m, z);
+                    } else {
+                        const float e = (vis && m != -INFINITY) ? exp2f(z - m) : 0.f;
+                        bsum += e;
+                        if ((key + 1) % p.G == 0 || key + 1 == k1) {
+                            if (valid) p.part[sq.part_off + (int64_t)(key / p.G) * sq.R + r] = bsum;
+                            lsum[((key - k0) / kTileKeys) % kSlotsPerChunk] += bsum;
+                            bsum = 0.f;
+                        }
+                    }
+                }
+            }
+        }
+        if (valid) {
+#pragma unroll
+            for (int sl = 0; sl < kSlotsPerChunk; ++sl) {
+                const int64_t o = sq.stat_off + (int64_t)(kSlotsPerChunk * c + sl) * sq.R + r;
+                p.mref[o] = m;
+                p.lsum[o] = lsum[sl];
+            }
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const ScoreParams &p, int num_sms, cudaStream_t st) {
+    const size_t smem = (size_t)D * kRowsPerTile * 2 + (size_t)kKeyTile * D * 4;
+    cudaError_t e = cudaFuncSetAttribute(score_fallback_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    score_fallback_kernel<D><<<num_sms, kRowsPerTile, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_score_fallback(const ScoreParams &p, int num_sms, cudaStream_t st) {
+    switch (p.d) {
+        case 64: return launch_d<64>(p, num_sms, st);
+        case 128: return launch_d<128>(p, num_sms, st);
+        case 256: return launch_d<256>(p, num_sms, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace up

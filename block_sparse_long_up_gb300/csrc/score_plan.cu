@@ -66,7 +66,7 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
     if (bad) {
         if (threadIdx.x == 0) {
             atomicOr(err, 0x1u);
-            cnt->units = 0; cnt->blocks = 0; cnt->rows = 0;
+            cnt->units = 0; cnt->blocks = 0; cnt->rows = 0; cnt->flagged = 0;
         }
         for (int s = threadIdx.x; s <= B; s += blockDim.x) cu_blocks[s] = 0;
         return;
@@ -90,7 +90,7 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
         const int64_t ou = block_excl_scan(units, &tu, sh);
         const int64_t orow = block_excl_scan(R, &tr, sh);
         const int64_t op = block_excl_scan(R * nb, &tp, sh);
-        const int64_t os = block_excl_scan(R * nch, &ts, sh);
+        const int64_t os = block_excl_scan(R * nch * kSlotsPerChunk, &ts, sh);
         if (s < B) {
             SeqInfo si;
             si.tok_off = cu[s];
@@ -116,6 +116,7 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
         cnt->units = (int32_t)base_u;
         cnt->blocks = (int32_t)base_b;
         cnt->rows = base_r;
+        cnt->flagged = 0;
     }
 }
 
@@ -138,7 +139,8 @@ __device__ __forceinline__ int find_seq_by_block(const SeqInfo *seqs, int B, int
 }
 
 // Per row: m = max_c mref, l = sum_c lsum_c * 2^(mref_c - m), and the weight of
-// chunk c: w_c = 2^(mref_c - m) / (l * R), R = n_s * Hq (the query/head mean).
+// statistics slot c: w_c = 2^(mref_c - m) / (l * R), R = n_s * Hq (the query/head
+// mean).  A slot holds the partial sums of every other key tile of a chunk.
 __global__ void __launch_bounds__(256)
 finalize_rows_kernel(ScoreParams p) {
     const int64_t total = p.counters->rows;
@@ -149,16 +151,17 @@ finalize_rows_kernel(ScoreParams p) {
         const int64_t r = gr - sq.row_off;
         const float *mr = p.mref + sq.stat_off + r;
         const float *ls = p.lsum + sq.stat_off + r;
+        const int nslots = sq.nchunks * kSlotsPerChunk;
         float m = -INFINITY;
-        for (int c = 0; c < sq.nchunks; ++c) m = fmaxf(m, mr[(int64_t)c * sq.R]);
+        for (int c = 0; c < nslots; ++c) m = fmaxf(m, mr[(int64_t)c * sq.R]);
         float l = 0.f;
-        for (int c = 0; c < sq.nchunks; ++c) {
+        for (int c = 0; c < nslots; ++c) {
             const float mc = mr[(int64_t)c * sq.R];
             if (mc != -INFINITY) l += ls[(int64_t)c * sq.R] * exp2f(mc - m);
         }
         const float inv = 1.0f / (l * (float)sq.R);
         float *w = p.w + sq.stat_off + r;
-        for (int c = 0; c < sq.nchunks; ++c) {
+        for (int c = 0; c < nslots; ++c) {
             const float mc = mr[(int64_t)c * sq.R];
             w[(int64_t)c * sq.R] = (mc == -INFINITY) ? 0.f : exp2f(mc - m) * inv;
         }
@@ -176,7 +179,7 @@ finalize_blocks_kernel(ScoreParams p) {
         const int s = find_seq_by_block(p.seqs, p.num_seqs, gb);
         const SeqInfo sq = p.seqs[s];
         const int b = gb - sq.blk_off;
-        const int c = (b * p.G) / p.C;
+        const int c = block_slot(b, p.G, p.C);
         const float *w = p.w + sq.stat_off + (int64_t)c * sq.R;
         const float *pt = p.part + sq.part_off + (int64_t)b * sq.R;
         float acc = 0.f;

@@ -204,3 +204,26 @@ def test_full_size_d256_sweep():
                     ox, opos, ocu, osrc = oracle.compact(inp.x, inp.pos, inp.cu_seqlens, G, gk, g_cb)
                     assert np.array_equal(xo, ox) and np.array_equal(src, osrc)
                     np.testing.assert_array_equal(cuo, ocu)
+
+
+def test_overflowing_unit_takes_the_exact_fallback():
+    """Keys 512..599 of KV head 0 are aligned with the queries' common direction
+    and scaled so their logits sit ~130 nats (~190 binary orders) above the
+    first key tile of their work unit.  The tensor-core kernel's fp32 sums for
+    that unit overflow; the unit must be queued and recomputed exactly."""
+    inp = synth.make_inputs([32768], 32, 8, 128, 128, 0.05, gain=5.0, hidden=64, seed=11)
+    qm = synth.bf16_bits_to_f32(inp.q_last).reshape(-1, 128).mean(axis=0)
+    qm /= np.linalg.norm(qm)
+    inp.k[512:600, 0, :] = synth.f32_to_bf16_bits(200.0 * qm)
+    q, k, cu = to_dev_bf16(inp.q_last), to_dev_bf16(inp.k), to_dev_i32(inp.cu_seqlens)
+    ws = torch.empty(up.score_blocks_workspace(1, 32768, 32, 8, 128, 128, 64),
+                     dtype=torch.uint8, device="cuda")
+    sc, cb = up.score_blocks(q, k, cu, 128, 64, workspace=ws)
+    torch.cuda.synchronize()
+    flagged = int(ws[256 + 16:256 + 20].view(torch.int32).item())
+    assert flagged > 0, "the overflowing unit was not queued for the fallback"
+    orc_sc, orc_cb = oracle.score_blocks(inp.q_last, inp.k, inp.cu_seqlens, 32, 8, 128, 128, 64)
+    g_sc = sc[: int(orc_cb[-1])].cpu().numpy().astype(np.float64)
+    nbad, worst = score_failures(g_sc, orc_sc)
+    assert nbad == 0, (nbad, worst)
+    assert up.get_device_error() == 0
