@@ -45,11 +45,13 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // Keys per work unit.  A function of the call's shape only (not of the GPU),
 // so scores are reproducible across devices: the largest power of two in
-// [256, 4096] that still yields >= 1024 work units.
+// [256, 4096] that still yields >= 1024 work units (several waves of CTAs,
+// so the last partial wave costs little).
 int choose_chunk(int B, int64_t total, int Hq, int Hk, int n) {
     const int g = Hq / Hk;
     const int64_t nn = n < total ? n : total;
-    const int64_t mt = (int64_t)Hk * ((g * nn + up::kRowsPerTile - 1) / up::kRowsPerTile);
+    const int64_t pair = (int64_t)up::kTilesPerUnit * up::kRowsPerTile;
+    const int64_t mt = (int64_t)Hk * ((g * nn + pair - 1) / pair);
     (void)B;
     for (int C = 4096; C > up::kChunkQuantum; C >>= 1)
         if (mt * (total / C) >= 1024) return C;
@@ -68,7 +70,8 @@ up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int n, int G)
     L.max_part = (int64_t)Hq * nn * L.max_blocks;
     const int64_t max_chunks = total / L.chunk + B;
     L.max_stat = (int64_t)Hq * nn * max_chunks * up::kSlotsPerChunk;
-    L.max_units = (int64_t)Hk * ((g * nn + up::kRowsPerTile - 1) / up::kRowsPerTile) * max_chunks;
+    const int64_t pair = (int64_t)up::kTilesPerUnit * up::kRowsPerTile;
+    L.max_units = (int64_t)Hk * ((g * nn + pair - 1) / pair) * max_chunks;
     size_t off = 0;
     L.seqs = off;     off = align256(off + sizeof(up::SeqInfo) * (size_t)(B > 0 ? B : 1));
     L.counters = off; off = align256(off + sizeof(up::Counters));

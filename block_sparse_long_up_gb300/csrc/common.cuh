@@ -17,7 +17,7 @@ struct SeqInfo {
     int32_t nb;        // ceil(L / G)
     int32_t blk_off;   // cu_blocks[s]
     int32_t nchunks;   // ceil(L / C): key chunks
-    int32_t mtiles;    // ceil(g * ns / 128): 128-row tiles per KV head
+    int32_t mtiles;    // ceil(g * ns / 256): 256-row tile pairs per KV head
     int32_t R;         // Hq * ns: softmax rows of the sequence
     int32_t unit_off;  // first score work unit of the sequence
     int64_t row_off;   // first global row (exclusive prefix of R)
@@ -37,16 +37,14 @@ struct Counters {
 static_assert(sizeof(Counters) == 64, "Counters is 64 bytes");
 
 constexpr int kRowsPerTile = 128;   // rows of one M tile (TMEM lanes)
-constexpr int kTileKeys = 256;      // keys of one MMA tile (N)
+constexpr int kTilesPerUnit = 2;    // M tiles a score CTA computes against each key step
+constexpr int kStepKeys = 128;      // keys of one MMA step (N)
 constexpr int kChunkQuantum = 256;  // key chunks are multiples of this (and of G)
-// Statistics slots per key chunk: the tiles of a chunk alternate between two
-// softmax warpgroups, and each keeps its own reference, so slot = tile parity.
-constexpr int kSlotsPerChunk = 2;
+constexpr int kSlotsPerChunk = 1;   // statistics slots per (row, key chunk)
 
-// Statistics slot of block b (G divides kTileKeys, C is a multiple of it).
+// Statistics slot of block b (C is a multiple of G).
 __host__ __device__ __forceinline__ int block_slot(int b, int G, int C) {
-    const int key = b * G;
-    return kSlotsPerChunk * (key / C) + ((key % C) / kTileKeys) % kSlotsPerChunk;
+    return kSlotsPerChunk * ((b * G) / C);
 }
 
 // Score workspace layout (offsets in bytes, every region 256-byte aligned).
@@ -67,7 +65,7 @@ struct ScoreParams {
     float *lsum;   // [c][r] per sequence: sum of the chunk's partials
     float *w;      // [c][r] per sequence: final weight of the chunk's partials
     float *scores;
-    int32_t *flag_list;  // units whose softmax sums overflowed (exact fallback)
+    int32_t *flag_list;  // 2*unit + M tile of tiles whose sums overflowed (exact fallback)
     int max_units;
     int flag_cap;        // capacity of flag_list
     int num_seqs, Hq, Hk, g, d, n, G, C;

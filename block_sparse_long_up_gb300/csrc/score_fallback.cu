@@ -1,14 +1,12 @@
 // score_simt.cu -- exact CUDA-core fallback for score work units.
 //
 // The tensor-core kernel measures every partial sum against a reference taken
-// from the first key tile its warpgroup sees in a work unit.  If a later tile of
-// the same unit holds logits more than ~115 binary orders of magnitude above
-// that reference, its fp32 sums overflow; the kernel then queues the unit here.
-// This kernel recomputes such a unit with two passes over the logits: the first
-// finds each row's exact maximum m over the unit's keys (log2 units), the
-// second sums 2^(z*log2e/sqrt(d) - m) over every block.  Both statistics slots
-// of the chunk get the same reference m; each gets the sum of the blocks of its
-// key tiles (even / odd tiles of the chunk).  The queue is empty for ordinary
+// from the first 32 keys of a work unit.  If a later key of the same unit has a
+// logit more than ~115 binary orders of magnitude above that reference, its fp32
+// sums overflow; the kernel then queues that 128-row tile here.  This kernel
+// recomputes such a tile with two passes over the logits: the first finds each
+// row's exact maximum m over the unit's keys (log2 units), the second sums
+// 2^(z*log2e/sqrt(d) - m) over every block.  The queue is empty for ordinary
 // attention logits.
 // Source: UniPrefill overview, block-wise importance estimation paragraph.
 #include "common.cuh"
@@ -40,11 +38,12 @@ score_fallback_kernel(ScoreParams p) {
     float *ks = reinterpret_cast<float *>(smem + D * kRowsPerTile * 2);          // [32][D]
     const int tid = threadIdx.x;
     for (int fi = blockIdx.x; fi < nflag; fi += gridDim.x) {
-        const int u = p.flag_list[fi];
+        const int entry = p.flag_list[fi];
+        const int u = entry >> 1;  // work unit; low bit: which of its two row tiles
         const int s = find_seq_by_unit(p.seqs, p.num_seqs, u);
         const SeqInfo sq = p.seqs[s];
         int loc = u - sq.unit_off;
-        const int mt = loc % sq.mtiles;
+        const int mt = (loc % sq.mtiles) * kTilesPerUnit + (entry & 1);
         loc /= sq.mtiles;
         const int c = loc % sq.nchunks;
         const int j = loc / sq.nchunks;
@@ -72,7 +71,7 @@ score_fallback_kernel(ScoreParams p) {
         const int k1 = min(k0 + p.C, sq.L);
         float m = -INFINITY;
         float acc[kKeyTile];
-        float lsum[kSlotsPerChunk] = {0.f, 0.f};
+        float lsum = 0.f;
         for (int pass = 0; pass < 2; ++pass) {
             float bsum = 0.f;
             for (int kt = k0; kt < k1; kt += kKeyTile) {
@@ -98,7 +97,7 @@ score_fallback_kernel(ScoreParams p) {
                         bsum += e;
                         if ((key + 1) % p.G == 0 || key + 1 == k1) {
                             if (valid) p.part[sq.part_off + (int64_t)(key / p.G) * sq.R + r] = bsum;
-                            lsum[((key - k0) / kTileKeys) % kSlotsPerChunk] += bsum;
+                            lsum += bsum;
                             bsum = 0.f;
                         }
                     }
@@ -106,12 +105,9 @@ score_fallback_kernel(ScoreParams p) {
             }
         }
         if (valid) {
-#pragma unroll
-            for (int sl = 0; sl < kSlotsPerChunk; ++sl) {
-                const int64_t o = sq.stat_off + (int64_t)(kSlotsPerChunk * c + sl) * sq.R + r;
-                p.mref[o] = m;
-                p.lsum[o] = lsum[sl];
-            }
+            const int64_t o = sq.stat_off + (int64_t)(kSlotsPerChunk * c) * sq.R + r;
+            p.mref[o] = m;
+            p.lsum[o] = lsum;
         }
     }
 }

@@ -4,6 +4,7 @@
 //   plan      (1 CTA)  cu_seqlens -> per-sequence table, cu_blocks, work-unit count.
 //   main      (score kernel) per (row, block) partial softmax sums relative to a
 //             per (row, chunk) reference, plus the chunk's reference and sum.
+//             A work unit is (sequence, KV head, pair of 128-row tiles, key chunk).
 //   finalize  rows:   per row, merge the chunk statistics into the row's softmax
 //                     normaliser and turn each chunk reference into a weight;
 //             blocks: per block, a fixed-order weighted sum over the sequence's
@@ -80,7 +81,7 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
             ns = L < n ? L : n;
             nb = (L + G - 1) / G;
             nch = (L + C - 1) / C;
-            mt = (g * ns + kRowsPerTile - 1) / kRowsPerTile;
+            mt = (g * ns + kTilesPerUnit * kRowsPerTile - 1) / (kTilesPerUnit * kRowsPerTile);
             R = (int64_t)Hq * ns;
             units = (int64_t)Hk * mt * nch;
         }
@@ -139,8 +140,7 @@ __device__ __forceinline__ int find_seq_by_block(const SeqInfo *seqs, int B, int
 }
 
 // Per row: m = max_c mref, l = sum_c lsum_c * 2^(mref_c - m), and the weight of
-// statistics slot c: w_c = 2^(mref_c - m) / (l * R), R = n_s * Hq (the query/head
-// mean).  A slot holds the partial sums of every other key tile of a chunk.
+// key chunk c: w_c = 2^(mref_c - m) / (l * R), R = n_s * Hq (the query/head mean).
 __global__ void __launch_bounds__(256)
 finalize_rows_kernel(ScoreParams p) {
     const int64_t total = p.counters->rows;

@@ -132,6 +132,20 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Same wait, with the loaded registers as in/out operands so that no use of
+// them can be scheduled before the data has arrived.
+__device__ __forceinline__ void tmem_wait_ld_dep(float (&v)[32]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+          "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]),
+          "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]), "+f"(v[18]), "+f"(v[19]),
+          "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]), "+f"(v[25]),
+          "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]), "+f"(v[31])
+        :
+        : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05.mma
 
 // Shared-memory matrix descriptor: K-major operand stored as 128-byte rows
@@ -174,6 +188,58 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 }
 
 // ---------------------------------------------------------------- math
+
+// packed fp32 pairs (two lanes of one 64-bit register)
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 2^x for two lanes on the FMA pipe (Cody-Waite range reduction + a degree-5
+// polynomial fitted to 2^f on [-1/2, 1/2] by iteratively reweighted least
+// squares on the relative error; max relative error ~2.4e-7 in fp32).
+// x is clamped at -127, so -inf gives ~2^-127 instead of 0.
+__device__ __forceinline__ uint64_t ex2_poly2(float x0, float x1) {
+    const uint64_t x = pack2(fmaxf(x0, -127.0f), fmaxf(x1, -127.0f));
+    const uint64_t t = add2(x, pack2(12582912.0f, 12582912.0f));      // 1.5*2^23: round to int
+    const uint64_t n = add2(t, pack2(-12582912.0f, -12582912.0f));
+    const uint64_t f = fma2(n, pack2(-1.0f, -1.0f), x);               // f = x - n in [-1/2, 1/2]
+    uint64_t q = fma2(pack2(1.3276379e-3f, 1.3276379e-3f), f, pack2(9.6755102e-3f, 9.6755102e-3f));
+    q = fma2(q, f, pack2(5.5507131e-2f, 5.5507131e-2f));
+    q = fma2(q, f, pack2(2.4022120e-1f, 2.4022120e-1f));
+    q = fma2(q, f, pack2(6.9314694e-1f, 6.9314694e-1f));
+    q = fma2(q, f, pack2(1.0000001f, 1.0000001f));
+    float q0, q1, t0, t1;
+    unpack2(q, q0, q1);
+    unpack2(t, t0, t1);
+    // scale by 2^n: the integer n sits in the low mantissa bits of t
+    const float r0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
+    const float r1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
+    return pack2(r0, r1);
+}
 
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

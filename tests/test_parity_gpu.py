@@ -34,6 +34,8 @@ def _lib():
     ([777], 2, 1, 128, 1, 64, 0.5, 5.0),                 # one query
     ([3000, 1500], 8, 2, 64, 128, 64, 0.99, None),       # literal unit shift: dense regime
     ([9000], 12, 4, 128, 48, 16, 0.999, 5.0),            # G=16, many blocks per chunk
+    ([300, 129, 4100], 4, 1, 64, 16, 256, 0.9, 5.0),     # G=256 block cut short by the sequence end
+    ([20000], 8, 1, 256, 96, 128, 0.95, 5.0),            # d=256, 768 rows = 1.5 tile pairs
 ])
 def test_small_shapes(lens, Hq, Hk, d, n, G, p, gain):
     inp = synth.make_inputs(lens, Hq, Hk, d, n, 0.05, gain=gain, hidden=64, seed=sum(lens) + d)
@@ -207,14 +209,17 @@ def test_full_size_d256_sweep():
 
 
 def test_overflowing_unit_takes_the_exact_fallback():
-    """Keys 512..599 of KV head 0 are aligned with the queries' common direction
-    and scaled so their logits sit ~130 nats (~190 binary orders) above the
-    first key tile of their work unit.  The tensor-core kernel's fp32 sums for
-    that unit overflow; the unit must be queued and recomputed exactly."""
+    """Among the first 4096 keys of KV head 0, those at positions 100..139 mod 256
+    are aligned with the queries' common direction and scaled so their logits
+    sit ~130 nats (~190 binary orders) above the other keys.  Work units start
+    at multiples of 256 keys, so these keys come after the keys a unit takes its
+    reference from; the tensor-core kernel's fp32 sums overflow, and the row
+    tiles must be queued and recomputed exactly."""
     inp = synth.make_inputs([32768], 32, 8, 128, 128, 0.05, gain=5.0, hidden=64, seed=11)
     qm = synth.bf16_bits_to_f32(inp.q_last).reshape(-1, 128).mean(axis=0)
     qm /= np.linalg.norm(qm)
-    inp.k[512:600, 0, :] = synth.f32_to_bf16_bits(200.0 * qm)
+    for base in range(0, 4096, 256):
+        inp.k[base + 100:base + 140, 0, :] = synth.f32_to_bf16_bits(200.0 * qm)
     q, k, cu = to_dev_bf16(inp.q_last), to_dev_bf16(inp.k), to_dev_i32(inp.cu_seqlens)
     ws = torch.empty(up.score_blocks_workspace(1, 32768, 32, 8, 128, 128, 64),
                      dtype=torch.uint8, device="cuda")
