@@ -211,7 +211,9 @@ def compact_noalloc(x, pos, cu_seqlens, G, keep, cu_blocks, x_out, pos_out, cu_s
 def get_device_error() -> int:
     """Read and clear the library's sticky device error bits (synchronises the device)."""
     v = ctypes.c_uint32(0)
-    lib().up_get_device_error(ctypes.byref(v))
+    st = lib().up_get_device_error(ctypes.byref(v))
+    if st not in (0, 5, 6):  # OK, or a device bit was set
+        raise UpError("up_get_device_error", st)
     return int(v.value)
 
 

@@ -78,7 +78,8 @@ up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int n, int G)
     L.part = off;     off = align256(off + sizeof(float) * (size_t)L.max_part);
     L.mref = off;     off = align256(off + sizeof(float) * (size_t)L.max_stat);
     L.lsum = off;     off = align256(off + sizeof(float) * (size_t)L.max_stat);
-    L.w = off;        off = align256(off + sizeof(float) * (size_t)L.max_stat);
+    L.rowm = off;     off = align256(off + sizeof(float) * (size_t)(L.max_rows > 0 ? L.max_rows : 1));
+    L.rowinv = off;   off = align256(off + sizeof(float) * (size_t)(L.max_rows > 0 ? L.max_rows : 1));
     L.flags = off;    off = align256(off + sizeof(int32_t) * (size_t)(16 * L.max_units + 16));
     L.total = off;
     return L;
@@ -183,7 +184,8 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     p.part = reinterpret_cast<float *>(ws + lay.part);
     p.mref = reinterpret_cast<float *>(ws + lay.mref);
     p.lsum = reinterpret_cast<float *>(ws + lay.lsum);
-    p.w = reinterpret_cast<float *>(ws + lay.w);
+    p.rowm = reinterpret_cast<float *>(ws + lay.rowm);
+    p.rowinv = reinterpret_cast<float *>(ws + lay.rowinv);
     p.scores = scores;
     p.flag_list = reinterpret_cast<int32_t *>(ws + lay.flags);
     p.max_units = (int)lay.max_units;

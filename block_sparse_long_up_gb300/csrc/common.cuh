@@ -49,7 +49,7 @@ __host__ __device__ __forceinline__ int block_slot(int b, int G, int C) {
 
 // Score workspace layout (offsets in bytes, every region 256-byte aligned).
 struct ScoreLayout {
-    size_t seqs, counters, part, mref, lsum, w, flags, total;
+    size_t seqs, counters, part, mref, lsum, rowm, rowinv, flags, total;
     int64_t max_part, max_stat, max_rows, max_units, max_blocks, total_tokens;
     int chunk;  // C: keys per work unit
 };
@@ -63,7 +63,8 @@ struct ScoreParams {
     float *part;   // [b][r] per sequence: block partial sums (relative to mref)
     float *mref;   // [c][r] per sequence: reference (log2 units) of the chunk's partials
     float *lsum;   // [c][r] per sequence: sum of the chunk's partials
-    float *w;      // [c][r] per sequence: final weight of the chunk's partials
+    float *rowm;   // [global row]: the row's softmax maximum (log2 units)
+    float *rowinv; // [global row]: 1 / (row softmax sum * n_s * Hq)
     float *scores;
     int32_t *flag_list;  // 2*unit + M tile of tiles whose sums overflowed (exact fallback)
     int max_units;

@@ -6,9 +6,10 @@
 //             per (row, chunk) reference, plus the chunk's reference and sum.
 //             A work unit is (sequence, KV head, pair of 128-row tiles, key chunk).
 //   finalize  rows:   per row, merge the chunk statistics into the row's softmax
-//                     normaliser and turn each chunk reference into a weight;
+//                     maximum and normaliser;
 //             blocks: per block, a fixed-order weighted sum over the sequence's
-//                     rows -> the block score.
+//                     rows (weight of a partial = 2^(chunk ref - row max) /
+//                     (normaliser * rows)) -> the block score.
 // UniPrefill overview, block-wise importance estimation paragraph: the block
 // score is the softmax attention mass of the last n queries that falls into a
 // block, averaged over queries and heads (the "online softmax" and "block
@@ -65,11 +66,15 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
     }
     bad = __syncthreads_or(bad);
     if (bad) {
+        // leave a well-formed empty plan: every later kernel sees no work
         if (threadIdx.x == 0) {
             atomicOr(err, 0x1u);
             cnt->units = 0; cnt->blocks = 0; cnt->rows = 0; cnt->flagged = 0;
         }
-        for (int s = threadIdx.x; s <= B; s += blockDim.x) cu_blocks[s] = 0;
+        for (int s = threadIdx.x; s <= B; s += blockDim.x) {
+            cu_blocks[s] = 0;
+            if (s < B) seqs[s] = SeqInfo{};
+        }
         return;
     }
     int64_t base_q = 0, base_b = 0, base_u = 0, base_r = 0, base_p = 0, base_s = 0;
@@ -130,63 +135,146 @@ __device__ __forceinline__ int find_seq_by_row(const SeqInfo *seqs, int B, int64
     return lo;
 }
 
-__device__ __forceinline__ int find_seq_by_block(const SeqInfo *seqs, int B, int b) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (seqs[mid].blk_off <= b) lo = mid; else hi = mid - 1;
-    }
-    return lo;
+// Row statistics.  Per row r of a sequence: m_r = max_c mref[c][r] and
+// l_r = sum_c lsum[c][r] * 2^(mref[c][r] - m_r); writes m_r and 1/(l_r * n_s * Hq)
+// (the softmax normaliser and the query/head mean).  A CTA takes 32 consecutive
+// rows; its 8 warps take every 8th chunk slot and merge (max, sum) online, then
+// warp 0 merges the 8 partial results in warp order -- a fixed order, so the
+// result is bitwise reproducible.
+constexpr int kRowsPerCta = 32;
+constexpr int kSlotLanes = 8;
+
+__device__ __forceinline__ void merge_ms(float &m, float &l, float mc, float lc) {
+    if (mc == -INFINITY) return;
+    if (m == -INFINITY) { m = mc; l = lc; return; }
+    const float mn = fmaxf(m, mc);
+    l = l * exp2f(m - mn) + lc * exp2f(mc - mn);
+    m = mn;
 }
 
-// Per row: m = max_c mref, l = sum_c lsum_c * 2^(mref_c - m), and the weight of
-// key chunk c: w_c = 2^(mref_c - m) / (l * R), R = n_s * Hq (the query/head mean).
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kRowsPerCta * kSlotLanes)
 finalize_rows_kernel(ScoreParams p) {
+    __shared__ float sm[kSlotLanes][kRowsPerCta], sl[kSlotLanes][kRowsPerCta];
     const int64_t total = p.counters->rows;
-    for (int64_t gr = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gr < total;
-         gr += (int64_t)gridDim.x * blockDim.x) {
-        const int s = find_seq_by_row(p.seqs, p.num_seqs, gr);
-        const SeqInfo sq = p.seqs[s];
-        const int64_t r = gr - sq.row_off;
-        const float *mr = p.mref + sq.stat_off + r;
-        const float *ls = p.lsum + sq.stat_off + r;
-        const int nslots = sq.nchunks * kSlotsPerChunk;
-        float m = -INFINITY;
-        for (int c = 0; c < nslots; ++c) m = fmaxf(m, mr[(int64_t)c * sq.R]);
-        float l = 0.f;
-        for (int c = 0; c < nslots; ++c) {
-            const float mc = mr[(int64_t)c * sq.R];
-            if (mc != -INFINITY) l += ls[(int64_t)c * sq.R] * exp2f(mc - m);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int64_t g0 = (int64_t)blockIdx.x * kRowsPerCta; g0 < total;
+         g0 += (int64_t)gridDim.x * kRowsPerCta) {
+        const int64_t gr = g0 + lane;
+        float m = -INFINITY, l = 0.f;
+        if (gr < total) {
+            const int s = find_seq_by_row(p.seqs, p.num_seqs, gr);
+            const SeqInfo sq = p.seqs[s];
+            const int64_t r = gr - sq.row_off;
+            const int nslots = sq.nchunks * kSlotsPerChunk;
+            const float *mr = p.mref + sq.stat_off + r;
+            const float *ls = p.lsum + sq.stat_off + r;
+            for (int c = wid; c < nslots; c += kSlotLanes)
+                merge_ms(m, l, mr[(int64_t)c * sq.R], ls[(int64_t)c * sq.R]);
         }
-        const float inv = 1.0f / (l * (float)sq.R);
-        float *w = p.w + sq.stat_off + r;
-        for (int c = 0; c < nslots; ++c) {
-            const float mc = mr[(int64_t)c * sq.R];
-            w[(int64_t)c * sq.R] = (mc == -INFINITY) ? 0.f : exp2f(mc - m) * inv;
+        sm[wid][lane] = m;
+        sl[wid][lane] = l;
+        __syncthreads();
+        if (wid == 0 && gr < total) {
+            float M = sm[0][lane], Lsum = sl[0][lane];
+#pragma unroll
+            for (int w = 1; w < kSlotLanes; ++w) merge_ms(M, Lsum, sm[w][lane], sl[w][lane]);
+            const int s = find_seq_by_row(p.seqs, p.num_seqs, gr);
+            const float R = (float)p.seqs[s].R;
+            p.rowm[gr] = M;
+            p.rowinv[gr] = (M == -INFINITY || !(Lsum > 0.f)) ? 0.f : 1.0f / (Lsum * R);
         }
+        __syncthreads();
     }
 }
 
-// One warp per block: score = sum_r w[c(b)][r] * part[b][r], lanes take rows
-// lane, lane+32, ... in order, then a fixed butterfly: bitwise reproducible.
-__global__ void __launch_bounds__(256)
+// Block scores.  A CTA takes one key chunk c of one sequence and up to 8 of its
+// blocks.  It first builds the chunk's row weights w[r] = 2^(mref[c][r] - m_r) * inv_r
+// in shared memory, then each warp reduces one block:
+//     score = sum_r part[b][r] * w[r]
+// lane i taking rows 4i.. (16-byte loads when the layout allows) into 4
+// interleaved accumulators, combined in a fixed order, then a fixed butterfly:
+// bitwise reproducible.
+constexpr int kBlocksPerCta = 8;
+constexpr int kMaxRowsSmem = 8192;
+
+__global__ void __launch_bounds__(kBlocksPerCta * 32)
 finalize_blocks_kernel(ScoreParams p) {
-    const int total = p.counters->blocks;
-    const int lane = threadIdx.x & 31;
-    const int warps = (gridDim.x * blockDim.x) >> 5;
-    for (int gb = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; gb < total; gb += warps) {
-        const int s = find_seq_by_block(p.seqs, p.num_seqs, gb);
+    __shared__ __align__(16) float w[kMaxRowsSmem];
+    if (p.counters->blocks <= 0) return;  // no valid plan (or nothing to do)
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int bpc = p.C / p.G;  // blocks per chunk
+    // CTA work item = (first block of a group of <= 8 blocks inside one chunk)
+    for (int it = blockIdx.x;; it += gridDim.x) {
+        // map it -> global block: groups never straddle a chunk or a sequence
+        const int groups_per_chunk = (bpc + kBlocksPerCta - 1) / kBlocksPerCta;
+        // walk sequences until the group index falls inside one
+        int rem = it, s = 0, found = 0;
+        for (; s < p.num_seqs; ++s) {
+            const int nch = p.seqs[s].nchunks;
+            const int ng = nch * groups_per_chunk;
+            if (rem < ng) { found = 1; break; }
+            rem -= ng;
+        }
+        if (!found) break;
         const SeqInfo sq = p.seqs[s];
-        const int b = gb - sq.blk_off;
-        const int c = block_slot(b, p.G, p.C);
-        const float *w = p.w + sq.stat_off + (int64_t)c * sq.R;
-        const float *pt = p.part + sq.part_off + (int64_t)b * sq.R;
-        float acc = 0.f;
-        for (int r = lane; r < sq.R; r += 32) acc = fmaf(__ldg(w + r), __ldcs(pt + r), acc);
+        const int c = rem / groups_per_chunk;
+        const int b_first = c * bpc + (rem % groups_per_chunk) * kBlocksPerCta;
+        const int b_last = min(min(b_first + kBlocksPerCta, (c + 1) * bpc), sq.nb);
+        if (b_first >= b_last) continue;  // a short last chunk has fewer blocks
+        const int slot = block_slot(b_first, p.G, p.C);
+        const float *mr = p.mref + sq.stat_off + (int64_t)slot * sq.R;
+        const float *rm = p.rowm + sq.row_off;
+        const float *ri = p.rowinv + sq.row_off;
+        const bool in_smem = sq.R <= kMaxRowsSmem;
+        __syncthreads();
+        if (in_smem)
+            for (int r = threadIdx.x; r < sq.R; r += blockDim.x)
+                w[r] = exp2f(__ldg(mr + r) - __ldg(rm + r)) * __ldg(ri + r);
+        __syncthreads();
+        const int b = b_first + wid;
+        if (b < b_last) {
+            const float *pt = p.part + sq.part_off + (int64_t)b * sq.R;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const bool vec = in_smem && (sq.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(pt) & 15) == 0);
+            if (vec) {
+                const float4 *pt4 = reinterpret_cast<const float4 *>(pt);
+                const float4 *w4 = reinterpret_cast<const float4 *>(w);
+                const int R4 = sq.R / 4;
+                int i = lane;
+                for (; i + 3 * 32 < R4; i += 4 * 32) {
+                    float4 x[4], y[4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) p.scores[gb] = acc;
+                    for (int k = 0; k < 4; ++k) x[k] = __ldcs(pt4 + i + k * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) y[k] = w4[i + k * 32];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        acc[k] = fmaf(x[k].x, y[k].x, acc[k]);
+                        acc[k] = fmaf(x[k].y, y[k].y, acc[k]);
+                        acc[k] = fmaf(x[k].z, y[k].z, acc[k]);
+                        acc[k] = fmaf(x[k].w, y[k].w, acc[k]);
+                    }
+                }
+                for (int k = 0; i < R4; i += 32, ++k) {
+                    const float4 x = __ldcs(pt4 + i), y = w4[i];
+                    float &a = acc[k & 3];
+                    a = fmaf(x.x, y.x, a);
+                    a = fmaf(x.y, y.y, a);
+                    a = fmaf(x.z, y.z, a);
+                    a = fmaf(x.w, y.w, a);
+                }
+            } else {
+                for (int r = lane, k = 0; r < sq.R; r += 32, ++k) {
+                    const float wr = in_smem ? w[r]
+                                             : exp2f(__ldg(mr + r) - __ldg(rm + r)) * __ldg(ri + r);
+                    acc[k & 3] = fmaf(__ldcs(pt + r), wr, acc[k & 3]);
+                }
+            }
+            float t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            if (lane == 0) p.scores[sq.blk_off + b] = t;
+        }
     }
 }
 
@@ -202,16 +290,20 @@ cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, con
 
 cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, cudaStream_t st) {
     if (lay.max_rows > 0) {
-        const int64_t want = (lay.max_rows + 255) / 256;
+        const int64_t want = (lay.max_rows + kRowsPerCta - 1) / kRowsPerCta;
         const int grid = (int)(want < 65535 ? want : 65535);
-        finalize_rows_kernel<<<grid, 256, 0, st>>>(p);
+        finalize_rows_kernel<<<grid, kRowsPerCta * kSlotLanes, 0, st>>>(p);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (lay.max_blocks > 0) {
-        const int64_t want = (lay.max_blocks + 7) / 8;  // 8 warps per CTA
+        // one CTA per group of <= 8 blocks inside a chunk (extra CTAs exit at once)
+        const int64_t bpc = p.C / p.G;
+        const int64_t groups = (bpc + kBlocksPerCta - 1) / kBlocksPerCta;
+        const int64_t max_chunks = lay.total_tokens / p.C + p.num_seqs;
+        const int64_t want = groups * max_chunks;
         const int grid = (int)(want < 65535 ? want : 65535);
-        finalize_blocks_kernel<<<grid, 256, 0, st>>>(p);
+        finalize_blocks_kernel<<<grid, kBlocksPerCta * 32, 0, st>>>(p);
         return cudaGetLastError();
     }
     return cudaSuccess;
