@@ -43,26 +43,35 @@ bool valid_G(int G) { return G == 16 || G == 32 || G == 64 || G == 128 || G == 2
 bool valid_d(int d) { return d == 64 || d == 128 || d == 256; }
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Keys per work unit.  A function of the call's shape only (not of the GPU),
-// so scores are reproducible across devices: the largest power of two in
-// [256, 4096] that still yields >= 1024 work units (several waves of CTAs,
-// so the last partial wave costs little).
-int choose_chunk(int B, int64_t total, int Hq, int Hk, int n) {
+// Keys per work unit (a multiple of 256).  The CTAs of the score kernel walk
+// the units round-robin, so the step count of the slowest CTA is
+// ceil(units / CTAs) * C; C is chosen to minimise that, plus a per-unit cost of
+// refilling the Q tiles (about 256 keys' worth), over C in 256..4096.  A function
+// of the call's shape and the device's SM count only, so scores are
+// reproducible on a given GPU model.
+int choose_chunk(int B, int64_t total, int Hq, int Hk, int d, int n, int ctas) {
     const int g = Hq / Hk;
     const int64_t nn = n < total ? n : total;
-    const int64_t pair = (int64_t)up::kTilesPerUnit * up::kRowsPerTile;
-    const int64_t mt = (int64_t)Hk * ((g * nn + pair - 1) / pair);
-    (void)B;
-    for (int C = 4096; C > up::kChunkQuantum; C >>= 1)
-        if (mt * (total / C) >= 1024) return C;
-    return up::kChunkQuantum;
+    const int64_t span = (int64_t)up::tiles_per_unit(d) * up::kRowsPerTile;
+    const int64_t groups = (int64_t)Hk * ((g * nn + span - 1) / span);
+    int best = up::kChunkQuantum;
+    int64_t best_cost = INT64_MAX;
+    for (int C = up::kChunkQuantum; C <= 4096; C += up::kChunkQuantum) {
+        const int64_t units = groups * ((total + C - 1) / C + (B > 1 ? B - 1 : 0));
+        const int64_t waves = (units + ctas - 1) / (ctas > 0 ? ctas : 1);
+        const int64_t cost = waves * (C + 256);
+        if (cost < best_cost) { best_cost = cost; best = C; }
+    }
+    return best;
 }
 
-up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int n, int G) {
+// Workspace layout for a given chunk size.  The smallest chunk needs the most
+// statistics, so sizing the workspace with C = 256 covers every chunk choice.
+up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int d, int n, int G, int chunk) {
     up::ScoreLayout L{};
     const int g = Hq / Hk;
     L.total_tokens = total;
-    L.chunk = choose_chunk(B, total, Hq, Hk, n);
+    L.chunk = chunk;
     const int64_t nn = n < total ? n : total;
     const int64_t ns_sum = ((int64_t)n * B < total) ? (int64_t)n * B : total;
     L.max_blocks = total / G + B;
@@ -70,8 +79,8 @@ up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int n, int G)
     L.max_part = (int64_t)Hq * nn * L.max_blocks;
     const int64_t max_chunks = total / L.chunk + B;
     L.max_stat = (int64_t)Hq * nn * max_chunks * up::kSlotsPerChunk;
-    const int64_t pair = (int64_t)up::kTilesPerUnit * up::kRowsPerTile;
-    L.max_units = (int64_t)Hk * ((g * nn + pair - 1) / pair) * max_chunks;
+    const int64_t span = (int64_t)up::tiles_per_unit(d) * up::kRowsPerTile;
+    L.max_units = (int64_t)Hk * ((g * nn + span - 1) / span) * max_chunks;
     size_t off = 0;
     L.seqs = off;     off = align256(off + sizeof(up::SeqInfo) * (size_t)(B > 0 ? B : 1));
     L.counters = off; off = align256(off + sizeof(up::Counters));
@@ -80,7 +89,7 @@ up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int n, int G)
     L.lsum = off;     off = align256(off + sizeof(float) * (size_t)L.max_stat);
     L.rowm = off;     off = align256(off + sizeof(float) * (size_t)(L.max_rows > 0 ? L.max_rows : 1));
     L.rowinv = off;   off = align256(off + sizeof(float) * (size_t)(L.max_rows > 0 ? L.max_rows : 1));
-    L.flags = off;    off = align256(off + sizeof(int32_t) * (size_t)(16 * L.max_units + 16));
+    L.flags = off;    off = align256(off + sizeof(int32_t) * (size_t)(32 * L.max_units + 16));
     L.total = off;
     return L;
 }
@@ -159,7 +168,7 @@ size_t up_score_blocks_workspace(int num_seqs, int64_t total_tokens, int Hq, int
                          d, n, G, reinterpret_cast<const float *>(16),
                          reinterpret_cast<const int32_t *>(16)) != UP_OK)
         return 0;
-    return score_layout(num_seqs, total_tokens, Hq, Hk, n, G).total;
+    return score_layout(num_seqs, total_tokens, Hq, Hk, d, n, G, up::kChunkQuantum).total;
 }
 
 up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_seqlens,
@@ -169,11 +178,14 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     up_status st = check_score_args(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n,
                                     G, scores, cu_blocks);
     if (st != UP_OK) return st;
-    const up::ScoreLayout lay = score_layout(num_seqs, total_tokens, Hq, Hk, n, G);
-    if (!workspace || workspace_bytes < lay.total || !aligned(workspace, 256))
+    if (!workspace || !aligned(workspace, 256) ||
+        workspace_bytes < score_layout(num_seqs, total_tokens, Hq, Hk, d, n, G, up::kChunkQuantum).total)
         return UP_ERR_WORKSPACE;
     DeviceState *ds = nullptr;
     if ((st = device_state(&ds)) != UP_OK) return st;
+    const int chunk = choose_chunk(num_seqs, total_tokens, Hq, Hk, d, n, ds->sms);
+    const up::ScoreLayout lay = score_layout(num_seqs, total_tokens, Hq, Hk, d, n, G, chunk);
+    if (workspace_bytes < lay.total) return UP_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
     up::ScoreParams p{};
@@ -189,7 +201,7 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     p.scores = scores;
     p.flag_list = reinterpret_cast<int32_t *>(ws + lay.flags);
     p.max_units = (int)lay.max_units;
-    p.flag_cap = (int)(16 * lay.max_units + 16);
+    p.flag_cap = (int)(32 * lay.max_units + 16);
     p.num_seqs = num_seqs;
     p.Hq = Hq; p.Hk = Hk; p.g = Hq / Hk; p.d = d; p.n = n; p.G = G; p.C = lay.chunk;
     p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));

@@ -17,7 +17,7 @@ struct SeqInfo {
     int32_t nb;        // ceil(L / G)
     int32_t blk_off;   // cu_blocks[s]
     int32_t nchunks;   // ceil(L / C): key chunks
-    int32_t mtiles;    // ceil(g * ns / 256): 256-row tile pairs per KV head
+    int32_t mtiles;    // ceil(g * ns / (128 * tiles_per_unit)): row-tile groups per KV head
     int32_t R;         // Hq * ns: softmax rows of the sequence
     int32_t unit_off;  // first score work unit of the sequence
     int64_t row_off;   // first global row (exclusive prefix of R)
@@ -37,8 +37,12 @@ struct Counters {
 static_assert(sizeof(Counters) == 64, "Counters is 64 bytes");
 
 constexpr int kRowsPerTile = 128;   // rows of one M tile (TMEM lanes)
-constexpr int kTilesPerUnit = 2;    // M tiles a score CTA computes against each key step
 constexpr int kStepKeys = 128;      // keys of one MMA step (N)
+
+// Row tiles a score CTA computes against each key step: all four tiles of a
+// 512-row GQA group share every K step in shared memory (head_dim <= 128); at
+// head_dim 256 the Q tiles of four would not fit next to the K ring, so two.
+__host__ __device__ constexpr int tiles_per_unit(int d) { return d <= 128 ? 4 : 2; }
 constexpr int kChunkQuantum = 256;  // key chunks are multiples of this (and of G)
 constexpr int kSlotsPerChunk = 1;   // statistics slots per (row, key chunk)
 
@@ -66,7 +70,7 @@ struct ScoreParams {
     float *rowm;   // [global row]: the row's softmax maximum (log2 units)
     float *rowinv; // [global row]: 1 / (row softmax sum * n_s * Hq)
     float *scores;
-    int32_t *flag_list;  // 2*unit + M tile of tiles whose sums overflowed (exact fallback)
+    int32_t *flag_list;  // 4*unit + row tile of tiles whose sums overflowed (exact fallback)
     int max_units;
     int flag_cap;        // capacity of flag_list
     int num_seqs, Hq, Hk, g, d, n, G, C;

@@ -39,11 +39,11 @@ score_fallback_kernel(ScoreParams p) {
     const int tid = threadIdx.x;
     for (int fi = blockIdx.x; fi < nflag; fi += gridDim.x) {
         const int entry = p.flag_list[fi];
-        const int u = entry >> 1;  // work unit; low bit: which of its two row tiles
+        const int u = entry >> 2;  // work unit; low two bits: which of its row tiles
         const int s = find_seq_by_unit(p.seqs, p.num_seqs, u);
         const SeqInfo sq = p.seqs[s];
         int loc = u - sq.unit_off;
-        const int mt = (loc % sq.mtiles) * kTilesPerUnit + (entry & 1);
+        const int mt = (loc % sq.mtiles) * tiles_per_unit(D) + (entry & 3);
         loc /= sq.mtiles;
         const int c = loc % sq.nchunks;
         const int j = loc / sq.nchunks;

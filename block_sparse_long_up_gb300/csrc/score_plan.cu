@@ -4,7 +4,7 @@
 //   plan      (1 CTA)  cu_seqlens -> per-sequence table, cu_blocks, work-unit count.
 //   main      (score kernel) per (row, block) partial softmax sums relative to a
 //             per (row, chunk) reference, plus the chunk's reference and sum.
-//             A work unit is (sequence, KV head, pair of 128-row tiles, key chunk).
+//             A work unit is (sequence, KV head, group of 128-row tiles, key chunk).
 //   finalize  rows:   per row, merge the chunk statistics into the row's softmax
 //                     maximum and normaliser;
 //             blocks: per block, a fixed-order weighted sum over the sequence's
@@ -52,7 +52,7 @@ __device__ int64_t block_excl_scan(int64_t v, int64_t *total, int64_t *sh) {
 __global__ void __launch_bounds__(kPlanThreads)
 score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_blocks,
                   SeqInfo *__restrict__ seqs, Counters *__restrict__ cnt, int B,
-                  int64_t total_tokens, int Hq, int Hk, int n, int G, int C,
+                  int64_t total_tokens, int Hq, int Hk, int d, int n, int G, int C,
                   unsigned int *err) {
     __shared__ int64_t sh[32];
     const int g = Hq / Hk;
@@ -86,7 +86,8 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
             ns = L < n ? L : n;
             nb = (L + G - 1) / G;
             nch = (L + C - 1) / C;
-            mt = (g * ns + kTilesPerUnit * kRowsPerTile - 1) / (kTilesPerUnit * kRowsPerTile);
+            const int64_t span = (int64_t)tiles_per_unit(d) * kRowsPerTile;
+            mt = (g * ns + span - 1) / span;
             R = (int64_t)Hq * ns;
             units = (int64_t)Hk * mt * nch;
         }
@@ -284,7 +285,7 @@ cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, con
                               int64_t total_tokens, cudaStream_t st) {
     score_plan_kernel<<<1, kPlanThreads, 0, st>>>(
         cu_seqlens, cu_blocks, const_cast<SeqInfo *>(p.seqs), const_cast<Counters *>(p.counters),
-        p.num_seqs, total_tokens, p.Hq, p.Hk, p.n, p.G, p.C, p.err);
+        p.num_seqs, total_tokens, p.Hq, p.Hk, p.d, p.n, p.G, p.C, p.err);
     return cudaGetLastError();
 }
 

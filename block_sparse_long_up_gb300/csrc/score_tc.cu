@@ -6,26 +6,30 @@
 // and heads.  Its fused-kernel paragraph names the pieces fused here: loads from
 // HBM, online softmax and block reduction in one pipeline.
 //
-// Work unit = (sequence s, KV head j, pair of 128-row tiles, key chunk c).  The
+// Work unit = (sequence s, KV head j, group of 128-row tiles, key chunk c).  The
 // rows are the packed GQA rows r = (query head h of group j, query t), so one K
 // step serves every query head that shares it (the PackGQA idea of the
-// FlashPrefill V2 review, re-derived for tcgen05), and one K panel in shared
-// memory feeds both row tiles, halving the K bytes each SM must stream per MMA.
+// FlashPrefill V2 review, re-derived for tcgen05).  A unit holds four row tiles
+// (512 rows: all query heads of a KV head at n = 128) when head_dim <= 128, so
+// each K byte enters shared memory once: on this GPU the TMA-to-shared-memory
+// path, not the tensor pipe, bounds a kernel that re-reads K per row tile.
 // A persistent CTA per SM walks its units; roles are warp-specialised:
 //   warp 0      TMA producer: 128-key x 64-dim K panels (128-byte swizzle) into
 //               a ring of shared-memory stages;
-//   warp 1      TMEM owner and MMA issuer: for each 128-key step, S = Q K^T for
-//               both row tiles (M=128, N=128 tcgen05.mma chains) into one of two
-//               TMEM buffers (2 steps x 2 tiles x 128 fp32 columns = 512);
-//   warps 2-3   Q loader: the unit's 256 packed query rows, swizzled into a
-//               K-major tile (double-buffered when shared memory allows);
-//   warps 4-11  two softmax warpgroups; warpgroup e owns row tile e.  Thread =
-//               row (TMEM lane).  It reads 32 columns at a time (the next
-//               group's TMEM load in flight while the current one is processed),
-//               applies the causal mask on the last steps, computes
-//               2^(z*log2e/sqrt(d) - ref) -- most on the MUFU, a fixed share with
-//               an FMA-pipe polynomial -- and sums each block of G keys; the
-//               block sums go straight to HBM as partials.
+//   warp 1      TMEM owner and MMA issuer: per 128-key step and per pair of row
+//               tiles, S = Q K^T (M=128, N=128 tcgen05.mma chains) into that
+//               pair's TMEM buffer (2 pairs x 2 tiles x 128 fp32 columns = 512),
+//               so one pair's softmax overlaps the other pair's MMAs;
+//   warps 2-3   Q loader: the unit's packed query rows, pair by pair, copied
+//               with cp.async into K-major swizzled tiles (one buffer per pair,
+//               two per pair when shared memory allows), so one pair's rows for
+//               the next unit load while the other pair still computes;
+//   warps 4-11  two softmax warpgroups; warpgroup e owns tile e of each pair.
+//               Thread = row (TMEM lane).  It reads 32 columns at a time (the
+//               next group's TMEM load in flight while the current one is
+//               processed), applies the causal mask on the last steps, computes
+//               2^(z*log2e/sqrt(d) - ref) on the MUFU and sums each block of G
+//               keys; the block sums go straight to HBM as partials.
 // The reference `ref` of a row is the largest visible logit among the first 32
 // keys of the unit; the row's statistics for the chunk (ref and the sum of all
 // its block partials) go to workspace.  Later keys may exceed ref; fp32 absorbs
@@ -53,25 +57,31 @@ constexpr int kEpiThreads = 128; // one warpgroup
 constexpr int kPanelBytesK = kStepKeys * 128;      // 128 keys x 64 bf16 = 16 KB
 constexpr int kPanelBytesQ = kRowsPerTile * 128;   // 128 rows x 64 bf16 = 16 KB
 constexpr uint32_t kTmemCols = 512;
+constexpr int kBufCols = 2 * kStepKeys;            // one TMEM buffer: a pair of tiles
 constexpr int kSmemBudget = 227 * 1024 - 2048;     // dynamic bytes we allow ourselves
 constexpr long long kWaitLimit = 4000000000LL;     // cycles, ~2 s
 constexpr int kMaxStages = 16;
 
 template <int D>
 struct Cfg {
+    static constexpr int kTiles = tiles_per_unit(D);
+    static constexpr int kPairs = kTiles / 2;
     static constexpr int kPanels = D / 64;
-    static constexpr int kQTileBytes = kPanels * kPanelBytesQ;           // one row tile
-    static constexpr int kQBytes = kTilesPerUnit * kQTileBytes;          // one Q buffer
+    static constexpr int kQTileBytes = kPanels * kPanelBytesQ;   // one row tile
+    static constexpr int kQPairBytes = 2 * kQTileBytes;          // the Q tiles of one pair
+    static constexpr int kQBytes = kTiles * kQTileBytes;         // one Q buffer (all pairs)
     static constexpr int kQBufs = (2 * kQBytes + 6 * kPanelBytesK <= kSmemBudget) ? 2 : 1;
+    static constexpr int kQSlots = kQBufs * kPairs;              // pair buffers
     static constexpr int kStagesFit = (kSmemBudget - 1024 - kQBufs * kQBytes) / kPanelBytesK;
     static constexpr int kStages = kStagesFit < kMaxStages ? kStagesFit : kMaxStages;
     static constexpr int kSmem = kQBufs * kQBytes + kStages * kPanelBytesK + 1024;
     static_assert(kStages >= kPanels, "at least one K step in flight");
+    static_assert(kTiles % 2 == 0 && kPairs <= 2, "tile pairs map onto the two TMEM buffers");
 };
 
 struct Shared {
     uint64_t kfull[kMaxStages], kempty[kMaxStages];
-    uint64_t qfull[2], qempty[2];
+    uint64_t qfull[4], qempty[4];  // one per pair buffer
     uint64_t tfull[2], tempty[2];
     uint64_t fin;
     uint32_t tmem_base;
@@ -80,14 +90,14 @@ struct Shared {
 
 struct Unit {
     SeqInfo sq;
-    int j, mp, c, k0, k1, nsteps;
+    int j, grp, c, k0, k1, nsteps;
 };
 
 __device__ __forceinline__ void decode_unit(const ScoreParams &p, int u, Unit &un) {
     const int s = find_seq_by_unit(p.seqs, p.num_seqs, u);
     un.sq = p.seqs[s];
     int loc = u - un.sq.unit_off;
-    un.mp = loc % un.sq.mtiles;  // row-tile pair
+    un.grp = loc % un.sq.mtiles;  // group of row tiles
     loc /= un.sq.mtiles;
     un.c = loc % un.sq.nchunks;
     un.j = loc / un.sq.nchunks;
@@ -137,102 +147,105 @@ aborted:
     }
 }
 
+// Q loader: for each unit and each pair of its row tiles, waits for the pair's
+// buffer, copies the rows with cp.async (all in flight at once; rows past the
+// group's end are zero-filled) in the K-major 128-byte-swizzled layout, and
+// hands the buffer to the MMA issuer.
 template <int D>
 __device__ void role_qload(const ScoreParams &p, Shared &sh, uint8_t *qbuf, int units) {
     using C = Cfg<D>;
     constexpr int kCh = D / 8;  // 16-byte chunks per row
-    constexpr int kTotal = kTilesPerUnit * kRowsPerTile * kCh;
-    constexpr int kBatch = 8;
+    constexpr int kTotal = 2 * kRowsPerTile * kCh;
     volatile int *abort = &sh.abort;
     const int qt = threadIdx.x - kWarpQ * 32;
     uint32_t ui = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++ui) {
         Unit un;
         decode_unit(p, u, un);
-        const int qb = ui % C::kQBufs;
-        const uint32_t use = ui / C::kQBufs;
-        if (!mbar_wait(smem_u32(&sh.qempty[qb]), (use & 1) ^ 1, abort, kWaitLimit)) return;
-        uint8_t *dst = qbuf + qb * C::kQBytes;
         const int ns = un.sq.ns;
         const int grows = p.g * ns;
-        const int row_base = un.mp * kTilesPerUnit * kRowsPerTile;
-        for (int base = qt; base < kTotal; base += kQThreads * kBatch) {
-            uint4 v[kBatch];
-#pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                const int idx = base + i * kQThreads;
-                v[i] = make_uint4(0, 0, 0, 0);
-                if (idx < kTotal) {
-                    const int row = idx / kCh, ch = idx % kCh;
-                    const int rr = row_base + row;
-                    if (rr < grows) {
-                        const int hh = rr / ns, tt = rr % ns;
-                        const __nv_bfloat16 *src =
-                            p.q + ((int64_t)(un.sq.q_off + tt) * p.Hq + un.j * p.g + hh) * D + ch * 8;
-                        v[i] = __ldg(reinterpret_cast<const uint4 *>(src));
-                    }
-                }
+        for (int pr = 0; pr < C::kPairs; ++pr) {
+            const int qs = (ui % C::kQBufs) * C::kPairs + pr;
+            const uint32_t use = ui / C::kQBufs;
+            if (!mbar_wait(smem_u32(&sh.qempty[qs]), (use & 1) ^ 1, abort, kWaitLimit)) return;
+            const uint32_t dst = smem_u32(qbuf + qs * C::kQPairBytes);
+            const int row_base = (un.grp * C::kTiles + 2 * pr) * kRowsPerTile;
+            for (int idx = qt; idx < kTotal; idx += kQThreads) {
+                const int row = idx / kCh, ch = idx % kCh;
+                const int tile = row / kRowsPerTile, tr = row % kRowsPerTile;
+                const int rr = row_base + row;
+                const bool ok = rr < grows;
+                const int hh = ok ? rr / ns : 0, tt = ok ? rr % ns : 0;
+                const __nv_bfloat16 *src =
+                    p.q + ((int64_t)(un.sq.q_off + tt) * p.Hq + un.j * p.g + hh) * D + ch * 8;
+                const int pn = ch >> 3, c16 = ch & 7;
+                cp_async16(dst + tile * C::kQTileBytes + pn * kPanelBytesQ + tr * 128 +
+                               ((c16 ^ (tr & 7)) << 4),
+                           ok ? (const void *)src : (const void *)p.q, ok ? 16u : 0u);
             }
-#pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                const int idx = base + i * kQThreads;
-                if (idx < kTotal) {
-                    const int row = idx / kCh, ch = idx % kCh;
-                    const int tile = row / kRowsPerTile, tr = row % kRowsPerTile;
-                    const int pn = ch >> 3, c16 = ch & 7;
-                    uint8_t *d = dst + tile * C::kQTileBytes + pn * kPanelBytesQ + tr * 128 +
-                                 ((c16 ^ (tr & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(d) = v[i];
-                }
-            }
+            cp_async_wait_all();
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&sh.qfull[qs]));
         }
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&sh.qfull[qb]));
     }
 }
 
+// MMA issue order: for each K step, pair 0 then pair 1 of the unit's row tiles.
+// Every (step, pair) is one "slot"; slot i uses TMEM buffer i % 2.  A K stage is
+// released once the last pair has consumed it.
 template <int D>
 __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_t *kbuf,
                          uint32_t tmem, int units) {
     using C = Cfg<D>;
     constexpr uint32_t idesc = idesc_bf16_f32(kRowsPerTile, kStepKeys);
     volatile int *abort = &sh.abort;
-    uint32_t it = 0, step = 0, ui = 0;
+    uint32_t it = 0, slot = 0, ui = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++ui) {
         Unit un;
         decode_unit(p, u, un);
-        const int qb = ui % C::kQBufs;
-        if (!mbar_wait(smem_u32(&sh.qfull[qb]), (ui / C::kQBufs) & 1, abort, kWaitLimit)) goto out;
-        tc_fence_after();
+        const int qs0 = (ui % C::kQBufs) * C::kPairs;
+        const uint32_t qph = (ui / C::kQBufs) & 1;
         {
-            const uint32_t qaddr = smem_u32(qbuf + qb * C::kQBytes);
-            for (int t = 0; t < un.nsteps; ++t, ++step) {
-                const int b = step & 1;
-                if (!mbar_wait(smem_u32(&sh.tempty[b]), ((step >> 1) & 1) ^ 1, abort, kWaitLimit))
-                    goto out;
-                tc_fence_after();
-                for (int pn = 0; pn < C::kPanels; ++pn, ++it) {
-                    const int st = it % C::kStages;
-                    if (!mbar_wait(smem_u32(&sh.kfull[st]), (it / C::kStages) & 1, abort, kWaitLimit))
+            for (int t = 0; t < un.nsteps; ++t) {
+                const uint32_t it0 = it;
+                for (int pr = 0; pr < C::kPairs; ++pr, ++slot) {
+                    const int b = slot & 1;
+                    if (t == 0) {
+                        if (!mbar_wait(smem_u32(&sh.qfull[qs0 + pr]), qph, abort, kWaitLimit)) goto out;
+                        tc_fence_after();
+                    }
+                    const uint32_t qaddr = smem_u32(qbuf + (qs0 + pr) * C::kQPairBytes);
+                    if (!mbar_wait(smem_u32(&sh.tempty[b]), ((slot >> 1) & 1) ^ 1, abort, kWaitLimit))
                         goto out;
                     tc_fence_after();
-                    const uint64_t bd = smem_desc_sw128(smem_u32(kbuf + st * kPanelBytesK));
+                    for (int pn = 0; pn < C::kPanels; ++pn) {
+                        const uint32_t i = it0 + pn;
+                        const int st = i % C::kStages;
+                        if (pr == 0) {
+                            if (!mbar_wait(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort,
+                                           kWaitLimit))
+                                goto out;
+                            tc_fence_after();
+                        }
+                        const uint64_t bd = smem_desc_sw128(smem_u32(kbuf + st * kPanelBytesK));
 #pragma unroll
-                    for (int e = 0; e < kTilesPerUnit; ++e) {
-                        const uint32_t d_tmem =
-                            tmem + (uint32_t)(b * kTilesPerUnit * kStepKeys + e * kStepKeys);
-                        const uint64_t ad =
-                            smem_desc_sw128(qaddr + e * C::kQTileBytes + pn * kPanelBytesQ);
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t d_tmem = tmem + (uint32_t)(b * kBufCols + e * kStepKeys);
+                            const uint64_t ad =
+                                smem_desc_sw128(qaddr + e * C::kQTileBytes + pn * kPanelBytesQ);
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)  // 4 x K=16 per 64-wide panel (32 B each)
-                            mma_bf16(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc, (pn | ks) != 0);
+                            for (int ks = 0; ks < 4; ++ks)  // 4 x K=16 per 64-wide panel (32 B)
+                                mma_bf16(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc, (pn | ks) != 0);
+                        }
+                        if (pr == C::kPairs - 1) mma_commit(smem_u32(&sh.kempty[st]));
                     }
-                    mma_commit(smem_u32(&sh.kempty[st]));
+                    mma_commit(smem_u32(&sh.tfull[b]));
+                    // the pair's Q tiles are free once its last step has run
+                    if (t == un.nsteps - 1) mma_commit(smem_u32(&sh.qempty[qs0 + pr]));
                 }
-                mma_commit(smem_u32(&sh.tfull[b]));
+                it = it0 + C::kPanels;
             }
         }
-        mma_commit(smem_u32(&sh.qempty[qb]));
     }
 out:
     // every MMA issued by this thread has completed once fin fires
@@ -240,11 +253,17 @@ out:
     mbar_drain(smem_u32(&sh.fin), 0);
 }
 
-// One 32-column group: scale, mask, exponentiate, and sum the two 16-column
-// halves.  Lane pairs (i, i+16) share one packed register so that the fixed
-// summation tree ends with (sum of columns 0..15, sum of 16..31).  Pairs 0..2
-// (6 of 32 values) are exponentiated on the FMA pipe, the rest on the MUFU.
-constexpr int kPolyPairs = 3;
+// One 32-column group: scale, mask, exponentiate, and return the sums of
+// columns 0..15 (lo) and 16..31 (hi) through a fixed summation tree.  The scale
+// and shift use packed fp32 FMAs on adjacent columns (which TMEM loads deliver
+// in register pairs); the exponentials run on the MUFU.
+__device__ __forceinline__ float sum16(const float *e) {
+    const float a0 = (e[0] + e[1]) + (e[2] + e[3]);
+    const float a1 = (e[4] + e[5]) + (e[6] + e[7]);
+    const float a2 = (e[8] + e[9]) + (e[10] + e[11]);
+    const float a3 = (e[12] + e[13]) + (e[14] + e[15]);
+    return (a0 + a1) + (a2 + a3);
+}
 
 __device__ __forceinline__ void group_exp_sums(float (&v)[32], bool masked, int key, int a,
                                                uint64_t s2, uint64_t bias2, float &lo, float &hi) {
@@ -252,127 +271,156 @@ __device__ __forceinline__ void group_exp_sums(float (&v)[32], bool masked, int 
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = (key + i > a) ? -INFINITY : v[i];
     }
-    uint64_t x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const uint64_t z = fma2(pack2(v[i], v[i + 16]), s2, bias2);
         float z0, z1;
-        unpack2(z, z0, z1);
-        x[i] = (i < kPolyPairs) ? ex2_poly2(z0, z1) : pack2(ex2_approx(z0), ex2_approx(z1));
+        unpack2(fma2(pack2(v[2 * i], v[2 * i + 1]), s2, bias2), z0, z1);
+        v[2 * i] = ex2_approx(z0);
+        v[2 * i + 1] = ex2_approx(z1);
+    }
+    lo = sum16(v);
+    hi = sum16(v + 16);
+}
+
+// Per-row state of one row tile within a unit.
+struct RowState {
+    float *part;  // partial sums of this row: part[b * R]
+    float ref, lsum, acc;
+    uint64_t bias2;
+    int a;        // causal limit (absolute key position)
+    int64_t r;    // row within the sequence
+    bool valid;
+};
+
+template <int G>
+__device__ __forceinline__ void softmax_tile(const Unit &un, RowState &rs, uint32_t taddr, int t,
+                                             uint64_t s2, float s, Shared &sh, int buf) {
+    constexpr int kGroups = kStepKeys / 32;
+    constexpr int kGroupsPerBlock = G >= 32 ? G / 32 : 1;
+    const SeqInfo &sq = un.sq;
+    const int skey = un.k0 + t * kStepKeys;  // first key of the step
+    const bool masked = skey + kStepKeys - 1 > sq.L - sq.ns;
+    float va[32], vb[32];
+    tmem_ld32(taddr, va);
+    tmem_wait_ld_dep(va);
+    if (t == 0) {
+        // visibility is a suffix cut: an all-masked first group means an
+        // all-masked row, which gets ref = -inf and contributes nothing
+        const int a = rs.a;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 30; i += 3)
+            mx = max3(mx, fmaxf((skey + i > a) ? -INFINITY : va[i],
+                                (skey + i + 1 > a) ? -INFINITY : va[i + 1]),
+                      (skey + i + 2 > a) ? -INFINITY : va[i + 2]);
+        mx = max3(mx, (skey + 30 > a) ? -INFINITY : va[30], (skey + 31 > a) ? -INFINITY : va[31]);
+        rs.ref = mx * s;
+        const float bias = (rs.ref == -INFINITY) ? -INFINITY : -rs.ref;
+        rs.bias2 = pack2(bias, bias);
     }
 #pragma unroll
-    for (int w = 8; w >= 1; w >>= 1) {
-#pragma unroll
-        for (int i = 0; i < w; ++i) x[i] = add2(x[2 * i], x[2 * i + 1]);
+    for (int cg = 0; cg < kGroups; ++cg) {
+        float(&cur)[32] = (cg & 1) ? vb : va;
+        float(&nxt)[32] = (cg & 1) ? va : vb;
+        if (cg + 1 < kGroups) tmem_ld32(taddr + (cg + 1) * 32, nxt);
+        float lo, hi;
+        const int kb = skey + cg * 32;
+        group_exp_sums(cur, masked, kb, rs.a, s2, rs.bias2, lo, hi);
+        if constexpr (G == 16) {
+            const int b = kb / 16;
+            if (rs.valid && b < sq.nb) rs.part[(int64_t)b * sq.R] = lo;
+            if (rs.valid && b + 1 < sq.nb) rs.part[(int64_t)(b + 1) * sq.R] = hi;
+            rs.lsum += lo;
+            rs.lsum += hi;
+        } else {
+            rs.acc += lo + hi;
+            if ((t * kGroups + cg + 1) % kGroupsPerBlock == 0) {
+                const int b = (kb + 32 - G) / G;
+                if (rs.valid && b < sq.nb) rs.part[(int64_t)b * sq.R] = rs.acc;
+                rs.lsum += rs.acc;
+                rs.acc = 0.f;
+            }
+        }
+        if (cg + 1 < kGroups) {
+            tmem_wait_ld_dep(nxt);
+            if (cg + 2 == kGroups) {
+                // this tile is in registers: hand the buffer back
+                tc_fence_before();
+                mbar_arrive(smem_u32(&sh.tempty[buf]));
+            }
+        }
     }
-    unpack2(x[0], lo, hi);
 }
 
 template <int D, int G>
 __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, int units) {
+    using C = Cfg<D>;
     constexpr int kGroups = kStepKeys / 32;
     constexpr int kGroupsPerBlock = G >= 32 ? G / 32 : 1;
     volatile int *abort = &sh.abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = (warp - kWarpEpi) >> 2;  // row tile of the pair
+    const int e = (warp - kWarpEpi) >> 2;  // tile of each pair
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
     const float s = p.scale_log2;
     const uint64_t s2 = pack2(s, s);
-    uint32_t step = 0;
+    uint32_t slot = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         Unit un;
         decode_unit(p, u, un);
         const SeqInfo &sq = un.sq;
         const int grows = p.g * sq.ns;
-        const int rl = (un.mp * kTilesPerUnit + e) * kRowsPerTile + row;
-        const bool valid = rl < grows;
-        const int a = sq.L - sq.ns + (valid ? rl % sq.ns : 0);  // causal limit of this row
-        const int64_t r = (int64_t)un.j * grows + rl;           // h * n_s + t
-        float *part = p.part + sq.part_off + r;
-        float lsum = 0.f, ref = -INFINITY, acc = 0.f;
-        uint64_t bias2 = 0;
-        for (int t = 0; t < un.nsteps; ++t, ++step) {
-            const int buf = step & 1;
-            const bool ok = mbar_wait(smem_u32(&sh.tfull[buf]), (step >> 1) & 1, abort, kWaitLimit);
-            __syncwarp();  // tcgen05.ld is warp-collective: reconverge after polling
-            if (!__all_sync(0xffffffffu, ok)) return;
-            tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
-                                   (uint32_t)(buf * kTilesPerUnit * kStepKeys + e * kStepKeys);
-            const int skey = un.k0 + t * kStepKeys;  // first key of the step
-            const bool masked = skey + kStepKeys - 1 > sq.L - sq.ns;
-            float va[32], vb[32];
-            tmem_ld32(taddr, va);
-            tmem_wait_ld_dep(va);
-            if (t == 0) {
-                // visibility is a suffix cut: an all-masked first group means an
-                // all-masked row, which gets ref = -inf and contributes nothing
-                float mx = -INFINITY;
+        RowState rs[C::kPairs];
 #pragma unroll
-                for (int i = 0; i < 30; i += 3)
-                    mx = max3(mx, fmaxf((skey + i > a) ? -INFINITY : va[i],
-                                        (skey + i + 1 > a) ? -INFINITY : va[i + 1]),
-                              (skey + i + 2 > a) ? -INFINITY : va[i + 2]);
-                mx = max3(mx, (skey + 30 > a) ? -INFINITY : va[30],
-                          (skey + 31 > a) ? -INFINITY : va[31]);
-                ref = mx * s;
-                const float bias = (ref == -INFINITY) ? -INFINITY : -ref;
-                bias2 = pack2(bias, bias);
+        for (int pr = 0; pr < C::kPairs; ++pr) {
+            const int rl = (un.grp * C::kTiles + 2 * pr + e) * kRowsPerTile + row;
+            rs[pr].valid = rl < grows;
+            rs[pr].a = sq.L - sq.ns + (rs[pr].valid ? rl % sq.ns : 0);
+            rs[pr].r = (int64_t)un.j * grows + rl;  // h * n_s + t
+            rs[pr].part = p.part + sq.part_off + rs[pr].r;
+            rs[pr].ref = -INFINITY;
+            rs[pr].lsum = 0.f;
+            rs[pr].acc = 0.f;
+            rs[pr].bias2 = 0;
+        }
+        for (int t = 0; t < un.nsteps; ++t) {
+#pragma unroll
+            for (int pr = 0; pr < C::kPairs; ++pr, ++slot) {
+                const int buf = slot & 1;
+                const bool ok =
+                    mbar_wait(smem_u32(&sh.tfull[buf]), (slot >> 1) & 1, abort, kWaitLimit);
+                __syncwarp();  // tcgen05.ld is warp-collective: reconverge after polling
+                if (!__all_sync(0xffffffffu, ok)) return;
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
+                                       (uint32_t)(buf * kBufCols + e * kStepKeys);
+                softmax_tile<G>(un, rs[pr], taddr, t, s2, s, sh, buf);
             }
+        }
 #pragma unroll
-            for (int cg = 0; cg < kGroups; ++cg) {
-                float(&cur)[32] = (cg & 1) ? vb : va;
-                float(&nxt)[32] = (cg & 1) ? va : vb;
-                if (cg + 1 < kGroups) tmem_ld32(taddr + (cg + 1) * 32, nxt);
-                float lo, hi;
-                const int kb = skey + cg * 32;
-                group_exp_sums(cur, masked, kb, a, s2, bias2, lo, hi);
-                if constexpr (G == 16) {
-                    const int b = kb / 16;
-                    if (valid && b < sq.nb) part[(int64_t)b * sq.R] = lo;
-                    if (valid && b + 1 < sq.nb) part[(int64_t)(b + 1) * sq.R] = hi;
-                    lsum += lo;
-                    lsum += hi;
-                } else {
-                    acc += lo + hi;
-                    if ((t * kGroups + cg + 1) % kGroupsPerBlock == 0) {
-                        const int b = (kb + 32 - G) / G;
-                        if (valid && b < sq.nb) part[(int64_t)b * sq.R] = acc;
-                        lsum += acc;
-                        acc = 0.f;
-                    }
-                }
-                if (cg + 1 < kGroups) {
-                    tmem_wait_ld_dep(nxt);
-                    if (cg + 2 == kGroups) {
-                        // this tile of the step is in registers: hand the buffer back
-                        tc_fence_before();
-                        mbar_arrive(smem_u32(&sh.tempty[buf]));
-                    }
+        for (int pr = 0; pr < C::kPairs; ++pr) {
+            RowState &st = rs[pr];
+            if constexpr (G > 32) {
+                // a block cut short by the end of the sequence
+                if ((un.nsteps * kGroups) % kGroupsPerBlock != 0) {
+                    const int b = (un.k0 + (un.nsteps * kGroups - 1) * 32) / G;
+                    if (st.valid && b < sq.nb) st.part[(int64_t)b * sq.R] = st.acc;
+                    st.lsum += st.acc;
+                    st.acc = 0.f;
                 }
             }
-        }
-        if constexpr (G > 32) {
-            // a block cut short by the end of the sequence
-            if ((un.nsteps * kGroups) % kGroupsPerBlock != 0) {
-                const int b = (un.k0 + (un.nsteps * kGroups - 1) * 32) / G;
-                if (valid && b < sq.nb) part[(int64_t)b * sq.R] = acc;
-                lsum += acc;
-                acc = 0.f;
+            if (st.valid) {
+                const int64_t o = sq.stat_off + (int64_t)(kSlotsPerChunk * un.c) * sq.R + st.r;
+                p.mref[o] = st.ref;
+                p.lsum[o] = st.lsum;
             }
-        }
-        if (valid) {
-            const int64_t o = sq.stat_off + (int64_t)(kSlotsPerChunk * un.c) * sq.R + r;
-            p.mref[o] = ref;
-            p.lsum[o] = lsum;
-        }
-        // fp32 overflow of the sums (logits far above the reference): queue this
-        // row tile of the unit for the exact fallback
-        const bool bad = valid && !(lsum <= 3.0e38f);
-        if (__any_sync(0xffffffffu, bad) && lane == 0) {
-            const int idx = atomicAdd(&const_cast<Counters *>(p.counters)->flagged, 1);
-            if (idx < p.flag_cap) p.flag_list[idx] = 2 * u + e;
+            // fp32 overflow of the sums (logits far above the reference): queue
+            // this row tile of the unit for the exact fallback
+            const bool bad = st.valid && !(st.lsum <= 3.0e38f);
+            if (__any_sync(0xffffffffu, bad) && lane == 0) {
+                const int idx = atomicAdd(&const_cast<Counters *>(p.counters)->flagged, 1);
+                if (idx < p.flag_cap) p.flag_list[idx] = 4 * u + 2 * pr + e;
+            }
         }
     }
 }
@@ -395,11 +443,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const ScoreParams p) {
             mbar_init(smem_u32(&sh.kfull[i]), 1);
             mbar_init(smem_u32(&sh.kempty[i]), 1);
         }
+        for (int q = 0; q < C::kQSlots; ++q) {
+            mbar_init(smem_u32(&sh.qfull[q]), kQThreads);
+            mbar_init(smem_u32(&sh.qempty[q]), 1);
+        }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&sh.qfull[b]), kQThreads);
-            mbar_init(smem_u32(&sh.qempty[b]), 1);
             mbar_init(smem_u32(&sh.tfull[b]), 1);
-            mbar_init(smem_u32(&sh.tempty[b]), kTilesPerUnit * kEpiThreads);
+            mbar_init(smem_u32(&sh.tempty[b]), 2 * kEpiThreads);
         }
         mbar_init(smem_u32(&sh.fin), 1);
         sh.abort = 0;
