@@ -139,6 +139,30 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def profiled_traffic(workload, d, G):
+    """DRAM bytes per launch of the scoring kernel from the committed ncu summary,
+    or None when the summary is for another workload or the kernel source has
+    changed since the counters were taken."""
+    import hashlib
+    if workload != "llama31_8b_128k" or d != 128 or G != 64:
+        return None
+    summary = os.path.join(ROOT, "profiles", "score_tc_llama31_8b_128k.md")
+    src = os.path.join(ROOT, "block_sparse_long_up_gb300", "csrc", "score_tc.cu")
+    try:
+        text = open(summary).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    fields = dict(line.split(":", 1) for line in text.splitlines()
+                  if line.startswith(("source_sha256_16:", "dram_bytes_per_launch:")))
+    if fields.get("source_sha256_16", "").strip() != sha:
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 
 def oracle_sample(inp, heads, queries, threads, G, p):
@@ -206,7 +230,7 @@ def run_reference(args, inp, w):
     return dict(metric=METRIC, value=value, unit=UNIT, impl="reference", n_gpus=args.gpus,
                 steps=args.steps, warmup=args.warmup, ms_per_step=t * 1e3 / frac,
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
-                data="synthetic", config=dict(workload=args.workload, gain=args.gain),
+                data="synthetic", config=workload_config(args, inp, w, 1),
                 cpu_baseline=dict(value=value, unit=UNIT, cores=used, kind="oracle",
                                   sample=sample),
                 e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
@@ -241,9 +265,19 @@ def max_over_ranks(v, world):
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def workload_config(args, inp, w, world):
+    return dict(workload=args.workload, tokens=inp.total_tokens, num_seqs=inp.num_seqs,
+                Hq=inp.Hq, Hk=inp.Hk, head_dim=inp.d, hidden=inp.hidden, n=inp.n, G=w["G"],
+                p=w["p"], gain=args.gain,
+                parallelism=f"replica x{world}" if world > 1 else "single",
+                l2="inputs larger than L2 (k %.0f MB, x %.0f MB > 129 MB); no flush"
+                   % (inp.k.nbytes / 1e6, (inp.x.nbytes if inp.x is not None else 0) / 1e6))
 
 
 def run_ours(args, inp, w, rank, world):
@@ -275,9 +309,14 @@ def run_ours(args, inp, w, rank, world):
     kept = int(sp.total_kept.item())
     kept_blocks = int(sp.keep[: int(sp.cu_blocks[-1].item())].sum().item())
 
-    # timed region: K steps; per-call events on the launching stream
+    # timed region: K steps; per-call events on the launching stream, plus a pair
+    # recorded by the library around its tensor-core scoring kernel
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for e in ev:
+        for x in e:
+            x.record(stream)  # creates the CUDA events before the timed region
+    torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     gpu_uuid = None
     try:
@@ -291,6 +330,7 @@ def run_ours(args, inp, w, rank, world):
     for i in range(K):
         e = ev[i]
         e[0].record(stream)
+        up.set_kernel_timing_events(e[4], e[5])
         up.score_blocks(q, k, cu, n, G, sp.scores, sp.cu_blocks, sp.ws_score)
         e[1].record(stream)
         up.select_topp(sp.scores, sp.cu_blocks, cu, G, p, sp.keep, sp.kept_tokens)
@@ -299,6 +339,7 @@ def run_ours(args, inp, w, rank, world):
                    sp.src_idx, sp.total_kept, sp.ws_compact)
         e[3].record(stream)
     end.record(stream)
+    up.set_kernel_timing_events(None, None)
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(world)
@@ -307,6 +348,7 @@ def run_ours(args, inp, w, rank, world):
     t_score = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     t_select = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     t_compact = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    t_kernel = statistics.mean(e[4].elapsed_time(e[5]) for e in ev)
     if up.get_device_error():
         raise RuntimeError("device error during the timed region")
 
@@ -335,27 +377,26 @@ def run_ours(args, inp, w, rank, world):
     wm = work_model(inp, G)
     peaks, peak_src = measured_peaks()
     tc_peak = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
-    achieved = wm["flops"] / (t_score * 1e-3) / 1e12
+    achieved = wm["flops"] / (t_kernel * 1e-3) / 1e12
+    traffic = profiled_traffic(args.workload, inp.d, w["G"])
     cbytes = compact_bytes(kept, inp.hidden)
     value = world * inp.total_tokens / (ms_step * 1e-3)
     out = dict(
         metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=K, warmup=args.warmup,
         ms_per_step=ms_step, higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="bf16", data="synthetic",
-        config=dict(workload=args.workload, tokens=inp.total_tokens, num_seqs=inp.num_seqs,
-                    Hq=inp.Hq, Hk=inp.Hk, head_dim=inp.d, hidden=inp.hidden, n=n, G=G, p=p,
-                    gain=args.gain, parallelism=f"replica x{world}" if world > 1 else "single",
-                    l2="inputs larger than L2 (k %.0f MB, x %.0f MB > 129 MB); no flush"
-                       % (inp.k.nbytes / 1e6, inp.x.nbytes / 1e6)),
+        config=workload_config(args, inp, w, world),
         clocks=clk,
         e2e=(dict(value=world * inp.total_tokens / e2e_s, unit=UNIT, h2d_bytes_per_step=h2d,
                   d2h_bytes_per_step=d2h, ms_per_step=e2e_s * 1e3) if e2e_s else None),
         gpu_launches=K * sp.launches_per_step(),
-        roofline=dict(kernel="up_score_blocks", bound="tensor", achieved=achieved, peak=tc_peak,
-                      unit="TFLOP/s", frac=achieved / tc_peak, traffic=None,
-                      peak_source=f"{peak_src} bf16 sustained",
-                      exp_rate_per_s=wm["exps"] / (t_score * 1e-3)),
-        calls_ms=dict(score=t_score, select=t_select, compact=t_compact),
+        roofline=dict(kernel="score_tc_kernel (tcgen05 scoring)", bound="tensor",
+                      achieved=achieved, peak=tc_peak, unit="TFLOP/s", frac=achieved / tc_peak,
+                      traffic=traffic, kernel_ms=t_kernel,
+                      algorithmic_bytes=wm["score_bytes"],
+                      peak_source=f"{peak_src} bf16 sustained (kernel timed inside a long loop)",
+                      exp_rate_per_s=wm["exps"] / (t_kernel * 1e-3)),
+        calls_ms=dict(score=t_score, score_kernel=t_kernel, select=t_select, compact=t_compact),
         compact_roofline=dict(bound="hbm", achieved=cbytes / (t_compact * 1e-3) / 1e9,
                               peak=float(peaks["hbm_gbs"]), unit="GB/s",
                               frac=cbytes / (t_compact * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
@@ -378,6 +419,7 @@ def main():
         inp = synth.make_workload(args.workload, gain=gain_of(args.gain))
         out = run_reference(args, inp, w)
         out["n_gpus"] = world
+        out["config"] = workload_config(args, inp, w, world)
         print(json.dumps(out), flush=True)
         return 0
     rank, world = dist_setup()

@@ -20,7 +20,7 @@ import torch
 from . import _build
 
 __all__ = ["build", "lib", "UpError", "score_blocks_workspace", "score_blocks", "select_topp",
-           "compact_workspace", "compact", "compact_noalloc", "get_device_error", "Sparsifier", "SELECT_MAX_BLOCKS"]
+           "compact_workspace", "compact", "compact_noalloc", "set_kernel_timing_events", "get_device_error", "Sparsifier", "SELECT_MAX_BLOCKS"]
 
 SELECT_MAX_BLOCKS = 16384
 _lib = None
@@ -61,6 +61,8 @@ def lib():
     L.up_compact.restype = I
     L.up_compact_noalloc.argtypes = [P, P, I, P, I, I64, I, P, P, P, P, P, P, P, P]
     L.up_compact_noalloc.restype = I
+    L.up_set_kernel_timing_events.argtypes = [P, P]
+    L.up_set_kernel_timing_events.restype = I
     L.up_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.up_get_device_error.restype = I
     _lib = L
@@ -206,6 +208,13 @@ def compact_noalloc(x, pos, cu_seqlens, G, keep, cu_blocks, x_out, pos_out, cu_s
                                   _stream(stream))
     _check("up_compact_noalloc", st)
     return x_out, pos_out, cu_seqlens_out, total_kept, src_idx
+
+
+def set_kernel_timing_events(start=None, stop=None):
+    """Record two torch.cuda.Event objects around the tensor-core scoring kernel
+    of every later score_blocks call on this thread (None, None to stop)."""
+    h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)
+    _check("up_set_kernel_timing_events", lib().up_set_kernel_timing_events(h(start), h(stop)))
 
 
 def get_device_error() -> int:

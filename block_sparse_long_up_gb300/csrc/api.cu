@@ -20,6 +20,9 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
+// optional events recorded around the tensor-core scoring kernel (per host thread)
+thread_local cudaEvent_t t_kernel_start = nullptr, t_kernel_stop = nullptr;
+
 up_status device_state(DeviceState **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return UP_ERR_CUDA;
@@ -126,6 +129,13 @@ const char *up_status_string(up_status status) {
     return "unknown status";
 }
 
+up_status up_set_kernel_timing_events(up_event_t start_event, up_event_t stop_event) {
+    if ((start_event == nullptr) != (stop_event == nullptr)) return UP_ERR_INVALID_ARG;
+    t_kernel_start = reinterpret_cast<cudaEvent_t>(start_event);
+    t_kernel_stop = reinterpret_cast<cudaEvent_t>(stop_event);
+    return UP_OK;
+}
+
 up_status up_get_device_error(uint32_t *bits) {
     if (!bits) return UP_ERR_INVALID_ARG;
     DeviceState *ds = nullptr;
@@ -209,7 +219,9 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     if (up::launch_score_plan(cu_seqlens, cu_blocks, p, total_tokens, s) != cudaSuccess)
         return UP_ERR_CUDA;
     if (num_seqs == 0 || total_tokens == 0) return UP_OK;
+    if (t_kernel_start && cudaEventRecord(t_kernel_start, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_main(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
+    if (t_kernel_stop && cudaEventRecord(t_kernel_stop, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_fallback(p, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_finalize(p, lay, s) != cudaSuccess) return UP_ERR_CUDA;
     return UP_OK;

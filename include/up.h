@@ -193,6 +193,17 @@ up_status up_compact_noalloc(const void *x, const int32_t *pos, int hidden,
                              int32_t *total_kept, up_stream_t stream);
 
 /*
+ * Instrumentation: when both events are non-NULL, every later up_score_blocks
+ * call made by this host thread records `start_event` immediately before its
+ * tensor-core scoring kernel and `stop_event` immediately after it, on the
+ * call's stream, so the caller can time that kernel alone with
+ * cudaEventElapsedTime.  Pass NULL, NULL to stop.  The events are cudaEvent_t
+ * handles owned by the caller.  Not part of the method; no page counterpart.
+ */
+typedef struct CUevent_st *up_event_t;
+up_status up_set_kernel_timing_events(up_event_t start_event, up_event_t stop_event);
+
+/*
  * Reads and clears the sticky device error word of the current device
  * (UP_DEVERR_* bits; 0 if none).  This call synchronises the device.
  * Returns UP_OK if no bit was set, UP_ERR_TIMEOUT if the timeout bit was set,
