@@ -313,9 +313,9 @@ def run_ours(args, inp, w, rank, world):
     # recorded by the library around its tensor-core scoring kernel
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
-    for e in ev:
-        for x in e:
-            x.record(stream)  # creates the CUDA events before the timed region
+    for pair in ev:
+        for event in pair:
+            event.record(stream)  # creates the CUDA events before the timed region
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     gpu_uuid = None
