@@ -49,17 +49,19 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // Keys per work unit (a multiple of 256).  The CTAs of the score kernel walk
 // the units round-robin, so the step count of the slowest CTA is
 // ceil(units / CTAs) * C; C is chosen to minimise that, plus a per-unit cost of
-// refilling the Q tiles (about 256 keys' worth), over C in 256..4096.  A function
+// refilling the Q tiles (about 256 keys' worth), over C in 256..16384.  A function
 // of the call's shape and the device's SM count only, so scores are
 // reproducible on a given GPU model.
+constexpr int kMaxChunk = 16384;
+
 int choose_chunk(int B, int64_t total, int Hq, int Hk, int d, int n, int ctas) {
     const int g = Hq / Hk;
     const int64_t nn = n < total ? n : total;
-    const int64_t span = (int64_t)up::tiles_per_unit(d) * up::kRowsPerTile;
-    const int64_t groups = (int64_t)Hk * ((g * nn + span - 1) / span);
+    const int64_t tpt = up::tokens_per_tile(g), tpu = up::tiles_per_unit(d);
+    const int64_t groups = (int64_t)Hk * (((nn + tpt - 1) / tpt + tpu - 1) / tpu);
     int best = up::kChunkQuantum;
     int64_t best_cost = INT64_MAX;
-    for (int C = up::kChunkQuantum; C <= 4096; C += up::kChunkQuantum) {
+    for (int C = up::kChunkQuantum; C <= kMaxChunk; C += up::kChunkQuantum) {
         const int64_t units = groups * ((total + C - 1) / C + (B > 1 ? B - 1 : 0));
         const int64_t waves = (units + ctas - 1) / (ctas > 0 ? ctas : 1);
         const int64_t cost = waves * (C + 256);
@@ -82,8 +84,9 @@ up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int d, int n,
     L.max_part = (int64_t)Hq * nn * L.max_blocks;
     const int64_t max_chunks = total / L.chunk + B;
     L.max_stat = (int64_t)Hq * nn * max_chunks * up::kSlotsPerChunk;
-    const int64_t span = (int64_t)up::tiles_per_unit(d) * up::kRowsPerTile;
-    L.max_units = (int64_t)Hk * ((g * nn + span - 1) / span) * max_chunks;
+    const int64_t tpt = up::tokens_per_tile(g), tpu = up::tiles_per_unit(d);
+    L.max_units = (int64_t)Hk * (((nn + tpt - 1) / tpt + tpu - 1) / tpu) * max_chunks;
+    L.max_qrows = ns_sum;
     size_t off = 0;
     L.seqs = off;     off = align256(off + sizeof(up::SeqInfo) * (size_t)(B > 0 ? B : 1));
     L.counters = off; off = align256(off + sizeof(up::Counters));
@@ -214,6 +217,7 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     p.flag_cap = (int)(32 * lay.max_units + 16);
     p.num_seqs = num_seqs;
     p.Hq = Hq; p.Hk = Hk; p.g = Hq / Hk; p.d = d; p.n = n; p.G = G; p.C = lay.chunk;
+    p.tpt = up::tokens_per_tile(p.g);
     p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
     p.err = ds->err;
     if (up::launch_score_plan(cu_seqlens, cu_blocks, p, total_tokens, s) != cudaSuccess)

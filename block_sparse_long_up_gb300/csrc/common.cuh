@@ -17,7 +17,7 @@ struct SeqInfo {
     int32_t nb;        // ceil(L / G)
     int32_t blk_off;   // cu_blocks[s]
     int32_t nchunks;   // ceil(L / C): key chunks
-    int32_t mtiles;    // ceil(g * ns / (128 * tiles_per_unit)): row-tile groups per KV head
+    int32_t mtiles;    // ceil(ceil(ns / tokens_per_tile) / tiles_per_unit): row-tile groups per KV head
     int32_t R;         // Hq * ns: softmax rows of the sequence
     int32_t unit_off;  // first score work unit of the sequence
     int64_t row_off;   // first global row (exclusive prefix of R)
@@ -39,6 +39,14 @@ static_assert(sizeof(Counters) == 64, "Counters is 64 bytes");
 constexpr int kRowsPerTile = 128;   // rows of one M tile (TMEM lanes)
 constexpr int kStepKeys = 128;      // keys of one MMA step (N)
 
+// Softmax rows of a sequence are numbered r = j * g * n_s + t * g + h for query
+// t (0..n_s-1) of query head j * g + h (h < g, the GQA group of KV head j):
+// token-major inside a group, so one row tile holds the g heads of
+// tokens_per_tile consecutive queries (the g heads of a query are adjacent in
+// q_last, and a tile is one tensor-map box per 64 head dims).  At most
+// 128 - g * tokens_per_tile rows of a tile stay unused when g is not a power of 2.
+__host__ __device__ constexpr int tokens_per_tile(int g) { return kRowsPerTile / g; }
+
 // Row tiles a score CTA computes against each key step: all four tiles of a
 // 512-row GQA group share every K step in shared memory (head_dim <= 128); at
 // head_dim 256 the Q tiles of four would not fit next to the K ring, so two.
@@ -55,6 +63,7 @@ __host__ __device__ __forceinline__ int block_slot(int b, int G, int C) {
 struct ScoreLayout {
     size_t seqs, counters, part, mref, lsum, rowm, rowinv, flags, total;
     int64_t max_part, max_stat, max_rows, max_units, max_blocks, total_tokens;
+    int64_t max_qrows;  // upper bound on the rows of q_last (sum of n_s)
     int chunk;  // C: keys per work unit
 };
 
@@ -74,6 +83,7 @@ struct ScoreParams {
     int max_units;
     int flag_cap;        // capacity of flag_list
     int num_seqs, Hq, Hk, g, d, n, G, C;
+    int tpt;           // tokens_per_tile(g)
     float scale_log2;  // log2(e) / sqrt(d)
     unsigned int *err;
 };

@@ -49,21 +49,20 @@ score_fallback_kernel(ScoreParams p) {
         const int j = loc / sq.nchunks;
 
         const int grows = p.g * sq.ns;
-        const int rl = mt * kRowsPerTile + tid;
-        const bool valid = rl < grows;
-        const int t = valid ? rl % sq.ns : 0;
-        const int a = sq.L - sq.ns + t;
-        const int64_t r = (int64_t)j * grows + rl;
+        // row tid of the tile: query t = mt * tpt + tid / g of query head j * g + h
+        const int tl = tid / p.g, h = tid - tl * p.g;
+        const int t = mt * p.tpt + tl;
+        const bool valid = tid < p.g * p.tpt && t < sq.ns;
+        const int a = sq.L - sq.ns + (valid ? t : 0);
+        const int64_t r = (int64_t)j * grows + (int64_t)t * p.g + h;
 
         __syncthreads();
         for (int idx = tid; idx < kRowsPerTile * D; idx += kRowsPerTile) {
             const int row = idx / D, cc = idx % D;
-            const int rr = mt * kRowsPerTile + row;
+            const int rtl = row / p.g, rh = row - rtl * p.g, rt = mt * p.tpt + rtl;
             __nv_bfloat16 v = __float2bfloat16(0.f);
-            if (rr < grows) {
-                const int hh = rr / sq.ns, tt = rr % sq.ns;
-                v = p.q[((int64_t)(sq.q_off + tt) * p.Hq + j * p.g + hh) * D + cc];
-            }
+            if (row < p.g * p.tpt && rt < sq.ns)
+                v = p.q[((int64_t)(sq.q_off + rt) * p.Hq + j * p.g + rh) * D + cc];
             qT[cc * kRowsPerTile + row] = v;
         }
 

@@ -86,8 +86,8 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
             ns = L < n ? L : n;
             nb = (L + G - 1) / G;
             nch = (L + C - 1) / C;
-            const int64_t span = (int64_t)tiles_per_unit(d) * kRowsPerTile;
-            mt = (g * ns + span - 1) / span;
+            const int64_t tpt = tokens_per_tile(g), tpu = tiles_per_unit(d);
+            mt = ((ns + tpt - 1) / tpt + tpu - 1) / tpu;
             R = (int64_t)Hq * ns;
             units = (int64_t)Hk * mt * nch;
         }

@@ -7,23 +7,23 @@
 // HBM, online softmax and block reduction in one pipeline.
 //
 // Work unit = (sequence s, KV head j, group of 128-row tiles, key chunk c).  The
-// rows are the packed GQA rows r = (query head h of group j, query t), so one K
-// step serves every query head that shares it (the PackGQA idea of the
-// FlashPrefill V2 review, re-derived for tcgen05).  A unit holds four row tiles
-// (512 rows: all query heads of a KV head at n = 128) when head_dim <= 128, so
-// each K byte enters shared memory once: on this GPU the TMA-to-shared-memory
-// path, not the tensor pipe, bounds a kernel that re-reads K per row tile.
+// rows are the packed GQA rows of KV head j (query t of head j*g + h is row
+// t*g + h), so one K step serves every query head that shares it (the PackGQA
+// idea of the FlashPrefill V2 review, re-derived for tcgen05).  A unit holds
+// four row tiles (512 rows: all query heads of a KV head at n = 128) when
+// head_dim <= 128, so each K byte enters shared memory once.  Tiles are handled
+// in pairs; the two TMEM buffers (2 tiles x 128 fp32 columns each) alternate
+// between pairs (head_dim <= 128: pair p always uses buffer p) or between K
+// steps (head_dim 256: one pair per unit).
 // A persistent CTA per SM walks its units; roles are warp-specialised:
-//   warp 0      TMA producer: 128-key x 64-dim K panels (128-byte swizzle) into
-//               a ring of shared-memory stages;
-//   warp 1      TMEM owner and MMA issuer: per 128-key step and per pair of row
-//               tiles, S = Q K^T (M=128, N=128 tcgen05.mma chains) into that
-//               pair's TMEM buffer (2 pairs x 2 tiles x 128 fp32 columns = 512),
-//               so one pair's softmax overlaps the other pair's MMAs;
-//   warps 2-3   Q loader: the unit's packed query rows, pair by pair, copied
-//               with cp.async into K-major swizzled tiles (one buffer per pair,
-//               two per pair when shared memory allows), so one pair's rows for
-//               the next unit load while the other pair still computes;
+//   warp 0      K producer: TMA loads of 128-key x 64-dim K panels (128-byte
+//               swizzle) into a ring of shared-memory stages;
+//   warp 2      Q producer: TMA loads of each pair's Q tiles (one 3-D box of
+//               g heads x 128/g queries x 64 dims per tile and panel);
+//   warps 1, 3  MMA issuers, one per TMEM buffer: S = Q K^T as M=128, N=128
+//               tcgen05.mma chains.  The tensor pipe's issue queue is shallow,
+//               so the bookkeeping of one issuer (barrier waits, commits) runs
+//               while the other one's MMAs keep the pipe busy;
 //   warps 4-11  two softmax warpgroups; warpgroup e owns tile e of each pair.
 //               Thread = row (TMEM lane).  It reads 32 columns at a time (the
 //               next group's TMEM load in flight while the current one is
@@ -48,10 +48,10 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 384;
-constexpr int kWarpTma = 0;
-constexpr int kWarpMma = 1;
-constexpr int kWarpQ = 2;        // warps 2 and 3
-constexpr int kQThreads = 64;
+constexpr int kWarpTmaK = 0;
+constexpr int kWarpMma0 = 1;     // issues the MMAs of TMEM buffer 0
+constexpr int kWarpTmaQ = 2;
+constexpr int kWarpMma1 = 3;     // issues the MMAs of TMEM buffer 1
 constexpr int kWarpEpi = 4;      // warps 4..11: two warpgroups
 constexpr int kEpiThreads = 128; // one warpgroup
 constexpr int kPanelBytesK = kStepKeys * 128;      // 128 keys x 64 bf16 = 16 KB
@@ -75,15 +75,19 @@ struct Cfg {
     static constexpr int kStagesFit = (kSmemBudget - 1024 - kQBufs * kQBytes) / kPanelBytesK;
     static constexpr int kStages = kStagesFit < kMaxStages ? kStagesFit : kMaxStages;
     static constexpr int kSmem = kQBufs * kQBytes + kStages * kPanelBytesK + 1024;
+    // issuers that read one K stage / one Q pair buffer
+    static constexpr int kStageUsers = kPairs == 2 ? 2 : 1;
+    static constexpr int kQUsers = kPairs == 2 ? 1 : 2;
     static_assert(kStages >= kPanels, "at least one K step in flight");
     static_assert(kTiles % 2 == 0 && kPairs <= 2, "tile pairs map onto the two TMEM buffers");
+    static_assert(kQSlots <= 4, "Q pair buffers");
 };
 
 struct Shared {
     uint64_t kfull[kMaxStages], kempty[kMaxStages];
     uint64_t qfull[4], qempty[4];  // one per pair buffer
     uint64_t tfull[2], tempty[2];
-    uint64_t fin;
+    uint64_t fin[2];
     uint32_t tmem_base;
     int abort;
 };
@@ -91,9 +95,12 @@ struct Shared {
 struct Unit {
     SeqInfo sq;
     int j, grp, c, k0, k1, nsteps;
+    int npairs;  // pairs of row tiles holding at least one query (a prefix of the pairs)
 };
 
+template <int D>
 __device__ __forceinline__ void decode_unit(const ScoreParams &p, int u, Unit &un) {
+    using C = Cfg<D>;
     const int s = find_seq_by_unit(p.seqs, p.num_seqs, u);
     un.sq = p.seqs[s];
     int loc = u - un.sq.unit_off;
@@ -104,6 +111,17 @@ __device__ __forceinline__ void decode_unit(const ScoreParams &p, int u, Unit &u
     un.k0 = un.c * p.C;
     un.k1 = min(un.k0 + p.C, un.sq.L);
     un.nsteps = (un.k1 - un.k0 + kStepKeys - 1) / kStepKeys;
+    const int left = un.sq.ns - un.grp * C::kTiles * p.tpt;  // > 0: the group holds queries
+    un.npairs = min(C::kPairs, (left + 2 * p.tpt - 1) / (2 * p.tpt));
+}
+
+// The query (relative to the sequence) a row tile's tensor-map box starts at.
+// A tile's own queries start at tile * tpt; the last tile of a sequence is
+// shifted back so that its box ends at the sequence's last query and never
+// reads past q_last (whose length only the device knows).  The shifted box's
+// leading rows repeat queries of the previous tile and count as unused.
+__device__ __forceinline__ int tile_box_query(const ScoreParams &p, int ns, int tile) {
+    return min(tile * p.tpt, ns - p.tpt);
 }
 
 // Waits for an operation already issued to finish, without looking at the
@@ -118,139 +136,150 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
 // ---------------------------------------------------------------- roles
 
 template <int D>
-__device__ void role_tma(const CUtensorMap *tmap, const ScoreParams &p, Shared &sh,
-                         uint8_t *kbuf, int units) {
+__device__ void role_tma_k(const CUtensorMap *tmap, const ScoreParams &p, Shared &sh,
+                           uint8_t *kbuf, int units) {
     using C = Cfg<D>;
     volatile int *abort = &sh.abort;
     uint32_t it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         Unit un;
-        decode_unit(p, u, un);
+        decode_unit<D>(p, u, un);
         for (int t = 0; t < un.nsteps; ++t) {
             const int row0 = un.sq.tok_off + un.k0 + t * kStepKeys;
             for (int pn = 0; pn < C::kPanels; ++pn, ++it) {
                 const int st = it % C::kStages;
                 const uint32_t ph = (it / C::kStages) & 1;
-                if (!mbar_wait(smem_u32(&sh.kempty[st]), ph ^ 1, abort, kWaitLimit)) goto aborted;
+                if (!mbar_wait(smem_u32(&sh.kempty[st]), ph ^ 1, abort, kWaitLimit)) goto done;
                 mbar_arrive_expect_tx(smem_u32(&sh.kfull[st]), kPanelBytesK);
                 tma_load_2d(smem_u32(kbuf + st * kPanelBytesK), tmap, un.j * D + pn * 64, row0,
                             smem_u32(&sh.kfull[st]));
             }
         }
     }
-    return;
-aborted:
-    // let the loads already issued land before the CTA can exit
+done:
+    if (!*abort) return;
+    // after an abort nobody consumes the loads already issued: let them land
+    // before the CTA can exit
     for (uint32_t k = 0; k < (uint32_t)C::kStages && k < it; ++k) {
         const uint32_t i = it - 1 - k;
         mbar_drain(smem_u32(&sh.kfull[i % C::kStages]), (i / C::kStages) & 1);
     }
 }
 
-// Q loader: for each unit and each pair of its row tiles, waits for the pair's
-// buffer, copies the rows with cp.async (all in flight at once; rows past the
-// group's end are zero-filled) in the K-major 128-byte-swizzled layout, and
-// hands the buffer to the MMA issuer.
+// Q producer: for each unit and each pair of its row tiles that holds queries,
+// waits for the pair's buffer and loads both tiles with one 3-D box per tile and
+// 64-dim panel: {64 dims, g heads, tpt queries} of q_last viewed as
+// [queries][Hq][d], which lands as 128-byte rows (row = query * g + head) in the
+// K-major 128-byte-swizzled layout the MMA reads.
 template <int D>
-__device__ void role_qload(const ScoreParams &p, Shared &sh, uint8_t *qbuf, int units) {
+__device__ void role_tma_q(const CUtensorMap *tmap, const ScoreParams &p, Shared &sh,
+                           uint8_t *qbuf, int units) {
     using C = Cfg<D>;
-    constexpr int kCh = D / 8;  // 16-byte chunks per row
-    constexpr int kTotal = 2 * kRowsPerTile * kCh;
     volatile int *abort = &sh.abort;
-    const int qt = threadIdx.x - kWarpQ * 32;
+    const uint32_t tx = (uint32_t)(2 * C::kPanels * 128 * p.g * p.tpt);
+    // per pair buffer qs: bit qs of `parity` = parity of the loads issued into it
+    // so far, bit qs of `used` = at least one load issued
+    uint32_t parity = 0u, used = 0u;
     uint32_t ui = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++ui) {
         Unit un;
-        decode_unit(p, u, un);
-        const int ns = un.sq.ns;
-        const int grows = p.g * ns;
-        for (int pr = 0; pr < C::kPairs; ++pr) {
+        decode_unit<D>(p, u, un);
+        for (int pr = 0; pr < un.npairs; ++pr) {
             const int qs = (ui % C::kQBufs) * C::kPairs + pr;
-            const uint32_t use = ui / C::kQBufs;
-            if (!mbar_wait(smem_u32(&sh.qempty[qs]), (use & 1) ^ 1, abort, kWaitLimit)) return;
-            const uint32_t dst = smem_u32(qbuf + qs * C::kQPairBytes);
-            const int row_base = (un.grp * C::kTiles + 2 * pr) * kRowsPerTile;
-            for (int idx = qt; idx < kTotal; idx += kQThreads) {
-                const int row = idx / kCh, ch = idx % kCh;
-                const int tile = row / kRowsPerTile, tr = row % kRowsPerTile;
-                const int rr = row_base + row;
-                const bool ok = rr < grows;
-                const int hh = ok ? rr / ns : 0, tt = ok ? rr % ns : 0;
-                const __nv_bfloat16 *src =
-                    p.q + ((int64_t)(un.sq.q_off + tt) * p.Hq + un.j * p.g + hh) * D + ch * 8;
-                const int pn = ch >> 3, c16 = ch & 7;
-                cp_async16(dst + tile * C::kQTileBytes + pn * kPanelBytesQ + tr * 128 +
-                               ((c16 ^ (tr & 7)) << 4),
-                           ok ? (const void *)src : (const void *)p.q, ok ? 16u : 0u);
+            if (!mbar_wait(smem_u32(&sh.qempty[qs]), ((parity >> qs) & 1u) ^ 1u, abort, kWaitLimit))
+                goto done;
+            mbar_arrive_expect_tx(smem_u32(&sh.qfull[qs]), tx);
+            for (int e = 0; e < 2; ++e) {
+                const int tile = un.grp * C::kTiles + 2 * pr + e;
+                const int z = un.sq.q_off + tile_box_query(p, un.sq.ns, tile);
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_3d(smem_u32(qbuf + qs * C::kQPairBytes + e * C::kQTileBytes +
+                                         pn * kPanelBytesQ),
+                                tmap, pn * 64, un.j * p.g, z, smem_u32(&sh.qfull[qs]));
             }
-            cp_async_wait_all();
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&sh.qfull[qs]));
+            parity ^= 1u << qs;
+            used |= 1u << qs;
         }
     }
+done:
+    if (!*abort) return;
+    // the latest load into each used buffer completes phase parity ^ 1
+    for (int qs = 0; qs < C::kQSlots; ++qs)
+        if ((used >> qs) & 1u) mbar_drain(smem_u32(&sh.qfull[qs]), ((parity >> qs) & 1u) ^ 1u);
 }
 
-// MMA issue order: for each K step, pair 0 then pair 1 of the unit's row tiles.
-// Every (step, pair) is one "slot"; slot i uses TMEM buffer i % 2.  A K stage is
-// released once the last pair has consumed it.
+// MMA issuer w (0 or 1) issues every MMA into TMEM buffer w.  Slot order (the
+// softmax warpgroups follow the same one): for each unit, each K step, each
+// pair holding queries.  head_dim <= 128: pair p uses buffer p, and both issuers
+// walk every K stage (waiting for it and releasing it, with or without MMAs) so
+// a stage is refilled only after both have released it.  head_dim 256 (one
+// pair): buffer = parity of the CTA-wide K step count, and each stage is used
+// and released by that step's issuer alone.
 template <int D>
 __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_t *kbuf,
-                         uint32_t tmem, int units) {
+                         uint32_t tmem, int units, int w) {
     using C = Cfg<D>;
     constexpr uint32_t idesc = idesc_bf16_f32(kRowsPerTile, kStepKeys);
     volatile int *abort = &sh.abort;
-    uint32_t it = 0, slot = 0, ui = 0;
+    uint32_t it = 0, gstep = 0, tuse = 0;  // K panels, K steps, uses of TMEM buffer w
+    uint32_t qpar = 0u;  // bit qs: parity of the Q loads into pair buffer qs so far
+    const uint32_t d_base = tmem + (uint32_t)(w * kBufCols);
+    uint32_t ui = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++ui) {
         Unit un;
-        decode_unit(p, u, un);
-        const int qs0 = (ui % C::kQBufs) * C::kPairs;
-        const uint32_t qph = (ui / C::kQBufs) & 1;
-        {
-            for (int t = 0; t < un.nsteps; ++t) {
-                const uint32_t it0 = it;
-                for (int pr = 0; pr < C::kPairs; ++pr, ++slot) {
-                    const int b = slot & 1;
-                    if (t == 0) {
-                        if (!mbar_wait(smem_u32(&sh.qfull[qs0 + pr]), qph, abort, kWaitLimit)) goto out;
-                        tc_fence_after();
-                    }
-                    const uint32_t qaddr = smem_u32(qbuf + (qs0 + pr) * C::kQPairBytes);
-                    if (!mbar_wait(smem_u32(&sh.tempty[b]), ((slot >> 1) & 1) ^ 1, abort, kWaitLimit))
+        decode_unit<D>(p, u, un);
+        const int qb = (ui % C::kQBufs) * C::kPairs;
+        const int qs = qb + (C::kPairs == 2 ? w : 0);  // the pair buffer this issuer reads
+        const bool pair_ok = (C::kPairs == 2 ? w : 0) < un.npairs;
+        bool q_ready = false;
+        for (int t = 0; t < un.nsteps; ++t, ++gstep) {
+            const uint32_t it0 = it;
+            it += C::kPanels;
+            const bool mine = C::kPairs == 2 ? pair_ok : ((gstep & 1u) == (uint32_t)w);
+            if (C::kPairs == 1 && !mine) continue;  // the other issuer's step and stages
+            if (mine) {
+                if (!q_ready) {
+                    if (!mbar_wait(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort, kWaitLimit))
                         goto out;
-                    tc_fence_after();
-                    for (int pn = 0; pn < C::kPanels; ++pn) {
-                        const uint32_t i = it0 + pn;
-                        const int st = i % C::kStages;
-                        if (pr == 0) {
-                            if (!mbar_wait(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort,
-                                           kWaitLimit))
-                                goto out;
-                            tc_fence_after();
-                        }
-                        const uint64_t bd = smem_desc_sw128(smem_u32(kbuf + st * kPanelBytesK));
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const uint32_t d_tmem = tmem + (uint32_t)(b * kBufCols + e * kStepKeys);
-                            const uint64_t ad =
-                                smem_desc_sw128(qaddr + e * C::kQTileBytes + pn * kPanelBytesQ);
-#pragma unroll
-                            for (int ks = 0; ks < 4; ++ks)  // 4 x K=16 per 64-wide panel (32 B)
-                                mma_bf16(d_tmem, ad + 2 * ks, bd + 2 * ks, idesc, (pn | ks) != 0);
-                        }
-                        if (pr == C::kPairs - 1) mma_commit(smem_u32(&sh.kempty[st]));
-                    }
-                    mma_commit(smem_u32(&sh.tfull[b]));
-                    // the pair's Q tiles are free once its last step has run
-                    if (t == un.nsteps - 1) mma_commit(smem_u32(&sh.qempty[qs0 + pr]));
+                    q_ready = true;
                 }
-                it = it0 + C::kPanels;
+                if (!mbar_wait(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, kWaitLimit))
+                    goto out;
+                tc_fence_after();
+            }
+            for (int pn = 0; pn < C::kPanels; ++pn) {
+                const uint32_t i = it0 + pn;
+                const int st = i % C::kStages;
+                if (!mbar_wait(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort, kWaitLimit))
+                    goto out;
+                if (mine) {
+                    tc_fence_after();
+                    const uint64_t bd = smem_desc_sw128(smem_u32(kbuf + st * kPanelBytesK));
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const uint64_t ad = smem_desc_sw128(smem_u32(
+                            qbuf + qs * C::kQPairBytes + e * C::kQTileBytes + pn * kPanelBytesQ));
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)  // 4 x K=16 per 64-wide panel (32 B)
+                            mma_bf16(d_base + (uint32_t)(e * kStepKeys), ad + 2 * ks, bd + 2 * ks,
+                                     idesc, (pn | ks) != 0);
+                    }
+                }
+                mma_commit(smem_u32(&sh.kempty[st]));
+            }
+            if (mine) {
+                mma_commit(smem_u32(&sh.tfull[w]));
+                ++tuse;
             }
         }
+        // the pair buffer is free once this issuer's MMAs on it have completed
+        if (C::kPairs == 1 || pair_ok) mma_commit(smem_u32(&sh.qempty[qs]));
+        for (int pr = 0; pr < un.npairs; ++pr) qpar ^= 1u << (qb + pr);
     }
 out:
     // every MMA issued by this thread has completed once fin fires
-    mma_commit(smem_u32(&sh.fin));
-    mbar_drain(smem_u32(&sh.fin), 0);
+    mma_commit(smem_u32(&sh.fin[w]));
+    mbar_drain(smem_u32(&sh.fin[w]), 0);
 }
 
 // One 32-column group: scale, mask, exponentiate, and return the sums of
@@ -362,35 +391,41 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
     const int e = (warp - kWarpEpi) >> 2;  // tile of each pair
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
+    // this thread's row of a tile: query tl of the box, head h of the group
+    const int tl = row / p.g, h = row - tl * p.g;
+    const bool row_used = row < p.g * p.tpt;
     const float s = p.scale_log2;
     const uint64_t s2 = pack2(s, s);
-    uint32_t slot = 0;
+    uint32_t gstep = 0, tpar = 0u;  // bit b: parity of the uses of TMEM buffer b so far
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         Unit un;
-        decode_unit(p, u, un);
+        decode_unit<D>(p, u, un);
         const SeqInfo &sq = un.sq;
         const int grows = p.g * sq.ns;
         RowState rs[C::kPairs];
 #pragma unroll
         for (int pr = 0; pr < C::kPairs; ++pr) {
-            const int rl = (un.grp * C::kTiles + 2 * pr + e) * kRowsPerTile + row;
-            rs[pr].valid = rl < grows;
-            rs[pr].a = sq.L - sq.ns + (rs[pr].valid ? rl % sq.ns : 0);
-            rs[pr].r = (int64_t)un.j * grows + rl;  // h * n_s + t
+            const int tile = un.grp * C::kTiles + 2 * pr + e;
+            const int tq = tile_box_query(p, sq.ns, tile) + tl;  // query of this row
+            rs[pr].valid = row_used && tq >= tile * p.tpt && tq < sq.ns;
+            rs[pr].a = sq.L - sq.ns + (rs[pr].valid ? tq : 0);
+            rs[pr].r = (int64_t)un.j * grows + (int64_t)tq * p.g + h;
             rs[pr].part = p.part + sq.part_off + rs[pr].r;
             rs[pr].ref = -INFINITY;
             rs[pr].lsum = 0.f;
             rs[pr].acc = 0.f;
             rs[pr].bias2 = 0;
         }
-        for (int t = 0; t < un.nsteps; ++t) {
+        for (int t = 0; t < un.nsteps; ++t, ++gstep) {
 #pragma unroll
-            for (int pr = 0; pr < C::kPairs; ++pr, ++slot) {
-                const int buf = slot & 1;
+            for (int pr = 0; pr < C::kPairs; ++pr) {
+                if (pr >= un.npairs) break;
+                const int buf = C::kPairs == 2 ? pr : (int)(gstep & 1u);
                 const bool ok =
-                    mbar_wait(smem_u32(&sh.tfull[buf]), (slot >> 1) & 1, abort, kWaitLimit);
+                    mbar_wait(smem_u32(&sh.tfull[buf]), (tpar >> buf) & 1u, abort, kWaitLimit);
                 __syncwarp();  // tcgen05.ld is warp-collective: reconverge after polling
                 if (!__all_sync(0xffffffffu, ok)) return;
+                tpar ^= 1u << buf;
                 tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
                                        (uint32_t)(buf * kBufCols + e * kStepKeys);
@@ -399,6 +434,7 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
         }
 #pragma unroll
         for (int pr = 0; pr < C::kPairs; ++pr) {
+            if (pr >= un.npairs) break;
             RowState &st = rs[pr];
             if constexpr (G > 32) {
                 // a block cut short by the end of the sequence
@@ -427,7 +463,8 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
-score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const ScoreParams p) {
+score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                const ScoreParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ Shared sh;
@@ -441,43 +478,46 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const ScoreParams p) {
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(smem_u32(&sh.kfull[i]), 1);
-            mbar_init(smem_u32(&sh.kempty[i]), 1);
+            mbar_init(smem_u32(&sh.kempty[i]), C::kStageUsers);
         }
         for (int q = 0; q < C::kQSlots; ++q) {
-            mbar_init(smem_u32(&sh.qfull[q]), kQThreads);
-            mbar_init(smem_u32(&sh.qempty[q]), 1);
+            mbar_init(smem_u32(&sh.qfull[q]), 1);
+            mbar_init(smem_u32(&sh.qempty[q]), C::kQUsers);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&sh.tfull[b]), 1);
             mbar_init(smem_u32(&sh.tempty[b]), 2 * kEpiThreads);
+            mbar_init(smem_u32(&sh.fin[b]), 1);
         }
-        mbar_init(smem_u32(&sh.fin), 1);
         sh.abort = 0;
         fence_mbar_init();
     }
-    if (warp == kWarpMma) {
+    if (warp == kWarpMma0) {
         tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == kWarpTma && lane == 0) tma_prefetch_desc(&tmap);
+    if (warp == kWarpTmaK && lane == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&qmap);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
-    if (warp == kWarpTma) {
-        if (lane == 0) role_tma<D>(&tmap, p, sh, kbuf, units);
-    } else if (warp == kWarpMma) {
-        if (lane == 0) role_mma<D>(p, sh, qbuf, kbuf, tmem, units);
-    } else if (warp < kWarpEpi) {
-        role_qload<D>(p, sh, qbuf, units);
+    if (warp == kWarpTmaK) {
+        if (lane == 0) role_tma_k<D>(&kmap, p, sh, kbuf, units);
+    } else if (warp == kWarpTmaQ) {
+        if (lane == 0) role_tma_q<D>(&qmap, p, sh, qbuf, units);
+    } else if (warp == kWarpMma0 || warp == kWarpMma1) {
+        if (lane == 0) role_mma<D>(p, sh, qbuf, kbuf, tmem, units, warp == kWarpMma0 ? 0 : 1);
     } else {
         role_softmax<D, G>(p, sh, tmem, units);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kWarpMma0) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -513,16 +553,35 @@ bool encode_k_map(CUtensorMap *tm, const ScoreParams &p, int64_t total_tokens) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// q_last viewed as a 3-D array [queries][Hq][d] (d innermost); one box = 64 head
+// dims x g query heads x tpt queries, with the 128-byte swizzle.  The query
+// extent is an upper bound on the rows of q_last (the exact count is only known
+// on the device); the kernel never addresses a query past its own sequence, and
+// coordinates below 0 read as zeros.
+bool encode_q_map(CUtensorMap *tm, const ScoreParams &p, int64_t max_qrows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.Hq,
+                                (cuuint64_t)(max_qrows > 0 ? max_qrows : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)p.d * 2, (cuuint64_t)p.Hq * p.d * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)p.tpt};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16 *>(p.q), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int G>
 cudaError_t launch_dg(const ScoreParams &p, const ScoreLayout &lay, int num_sms, cudaStream_t st) {
-    CUtensorMap tm;
-    if (!encode_k_map(&tm, p, lay.total_tokens)) return cudaErrorInvalidValue;
+    CUtensorMap km, qm;
+    if (!encode_k_map(&km, p, lay.total_tokens)) return cudaErrorInvalidValue;
+    if (!encode_q_map(&qm, p, lay.max_qrows)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<D, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t grid = lay.max_units < num_sms ? lay.max_units : num_sms;
     if (grid < 1) return cudaSuccess;
-    score_tc_kernel<D, G><<<(unsigned)grid, kThreads, Cfg<D>::kSmem, st>>>(tm, p);
+    score_tc_kernel<D, G><<<(unsigned)grid, kThreads, Cfg<D>::kSmem, st>>>(km, qm, p);
     return cudaGetLastError();
 }
 
