@@ -282,33 +282,43 @@ out:
     mbar_drain(smem_u32(&sh.fin[w]), 0);
 }
 
-// One 32-column group: scale, mask, exponentiate, and return the sums of
-// columns 0..15 (lo) and 16..31 (hi) through a fixed summation tree.  The scale
-// and shift use packed fp32 FMAs on adjacent columns (which TMEM loads deliver
-// in register pairs); the exponentials run on the MUFU.
-__device__ __forceinline__ float sum16(const float *e) {
-    const float a0 = (e[0] + e[1]) + (e[2] + e[3]);
-    const float a1 = (e[4] + e[5]) + (e[6] + e[7]);
-    const float a2 = (e[8] + e[9]) + (e[10] + e[11]);
-    const float a3 = (e[12] + e[13]) + (e[14] + e[15]);
-    return (a0 + a1) + (a2 + a3);
-}
-
-__device__ __forceinline__ void group_exp_sums(float (&v)[32], bool masked, int key, int a,
-                                               uint64_t s2, uint64_t bias2, float &lo, float &hi) {
-    if (masked) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = (key + i > a) ? -INFINITY : v[i];
-    }
+// One 32-column group: scale, shift, exponentiate, and return the sums of
+// columns 0..15 (lo) and 16..31 (hi).  The scale and shift use packed fp32 FMAs
+// on adjacent columns (which TMEM loads deliver in register pairs), the
+// exponentials run on the MUFU, and the sums are a fixed tree of packed adds
+// (even and odd columns apart until the last add): bitwise reproducible.
+__device__ __forceinline__ void exp_sums(float (&v)[32], uint64_t s2, uint64_t bias2, float &lo,
+                                         float &hi) {
+    uint64_t e[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         float z0, z1;
         unpack2(fma2(pack2(v[2 * i], v[2 * i + 1]), s2, bias2), z0, z1);
-        v[2 * i] = ex2_approx(z0);
-        v[2 * i + 1] = ex2_approx(z1);
+        e[i] = pack2(ex2_approx(z0), ex2_approx(z1));
     }
-    lo = sum16(v);
-    hi = sum16(v + 16);
+    const uint64_t l = add2(add2(add2(e[0], e[1]), add2(e[2], e[3])),
+                            add2(add2(e[4], e[5]), add2(e[6], e[7])));
+    const uint64_t h = add2(add2(add2(e[8], e[9]), add2(e[10], e[11])),
+                            add2(add2(e[12], e[13]), add2(e[14], e[15])));
+    float x, y;
+    unpack2(l, x, y);
+    lo = x + y;
+    unpack2(h, x, y);
+    hi = x + y;
+}
+
+// Causal mask of one group: keys past the row's limit a contribute nothing.
+__device__ __forceinline__ void mask_group(float (&v)[32], int key, int a) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = (key + i > a) ? -INFINITY : v[i];
+}
+
+// One predicated store (no branch, so the group code stays one basic block).
+__device__ __forceinline__ void st_if(float *p, float v, bool ok) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.global.f32 [%0], %1;\n\t}" ::"l"(p),
+        "f"(v), "r"((int)ok)
+        : "memory");
 }
 
 // Per-row state of one row tile within a unit.
@@ -321,6 +331,9 @@ struct RowState {
     bool valid;
 };
 
+// A K step of one row tile, general case: the unit's first step (which sets
+// the reference) and the steps that reach the causal limit or the end of the
+// sequence (masked, and their blocks may run past the sequence's last one).
 template <int G>
 __device__ __forceinline__ void softmax_tile(const Unit &un, RowState &rs, uint32_t taddr, int t,
                                              uint64_t s2, float s, Shared &sh, int buf) {
@@ -354,18 +367,19 @@ __device__ __forceinline__ void softmax_tile(const Unit &un, RowState &rs, uint3
         if (cg + 1 < kGroups) tmem_ld32(taddr + (cg + 1) * 32, nxt);
         float lo, hi;
         const int kb = skey + cg * 32;
-        group_exp_sums(cur, masked, kb, rs.a, s2, rs.bias2, lo, hi);
+        if (masked) mask_group(cur, kb, rs.a);
+        exp_sums(cur, s2, rs.bias2, lo, hi);
         if constexpr (G == 16) {
             const int b = kb / 16;
-            if (rs.valid && b < sq.nb) rs.part[(int64_t)b * sq.R] = lo;
-            if (rs.valid && b + 1 < sq.nb) rs.part[(int64_t)(b + 1) * sq.R] = hi;
+            st_if(rs.part + (int64_t)b * sq.R, lo, rs.valid && b < sq.nb);
+            st_if(rs.part + (int64_t)(b + 1) * sq.R, hi, rs.valid && b + 1 < sq.nb);
             rs.lsum += lo;
             rs.lsum += hi;
         } else {
             rs.acc += lo + hi;
             if ((t * kGroups + cg + 1) % kGroupsPerBlock == 0) {
                 const int b = (kb + 32 - G) / G;
-                if (rs.valid && b < sq.nb) rs.part[(int64_t)b * sq.R] = rs.acc;
+                st_if(rs.part + (int64_t)b * sq.R, rs.acc, rs.valid && b < sq.nb);
                 rs.lsum += rs.acc;
                 rs.acc = 0.f;
             }
@@ -374,6 +388,54 @@ __device__ __forceinline__ void softmax_tile(const Unit &un, RowState &rs, uint3
             tmem_wait_ld_dep(nxt);
             if (cg + 2 == kGroups) {
                 // this tile is in registers: hand the buffer back
+                tc_fence_before();
+                mbar_arrive(smem_u32(&sh.tempty[buf]));
+            }
+        }
+    }
+}
+
+// A K step of one row tile, common case: not the unit's first, no key past the
+// causal limit (so every block it touches lies inside the sequence).  No
+// branch inside, so the compiler can overlap one group's sums with the next
+// group's exponentials.  skey is a multiple of 128 and of G when G <= 128; a
+// 256-key block closes at the end of every second step of the unit.
+template <int G>
+__device__ __forceinline__ void softmax_tile_fast(RowState &rs, uint32_t taddr, int skey, int t,
+                                                  int R, uint64_t s2, Shared &sh, int buf) {
+    constexpr int kGroups = kStepKeys / 32;
+    constexpr int kGroupsPerBlock = G >= 32 ? G / 32 : 1;
+    float *const pb = rs.part + (int64_t)(skey / G) * R;  // the step's first block
+    float va[32], vb[32];
+    tmem_ld32(taddr, va);
+    tmem_wait_ld_dep(va);
+#pragma unroll
+    for (int cg = 0; cg < kGroups; ++cg) {
+        float(&cur)[32] = (cg & 1) ? vb : va;
+        float(&nxt)[32] = (cg & 1) ? va : vb;
+        if (cg + 1 < kGroups) tmem_ld32(taddr + (cg + 1) * 32, nxt);
+        float lo, hi;
+        exp_sums(cur, s2, rs.bias2, lo, hi);
+        if constexpr (G == 16) {
+            st_if(pb + (int64_t)(2 * cg) * R, lo, rs.valid);
+            st_if(pb + (int64_t)(2 * cg + 1) * R, hi, rs.valid);
+            rs.lsum += lo;
+            rs.lsum += hi;
+        } else {
+            rs.acc += lo + hi;
+            const bool closes = G <= 128 ? ((cg + 1) % kGroupsPerBlock == 0)
+                                         : (cg + 1 == kGroups && (t & 1));
+            if (closes) {
+                // the closing block's index relative to the step's first block
+                const int off = G <= 128 ? ((cg + 1) * 32 / G - 1) : 0;
+                st_if(pb + (int64_t)off * R, rs.acc, rs.valid);
+                rs.lsum += rs.acc;
+                rs.acc = 0.f;
+            }
+        }
+        if (cg + 1 < kGroups) {
+            tmem_wait_ld_dep(nxt);
+            if (cg + 2 == kGroups) {
                 tc_fence_before();
                 mbar_arrive(smem_u32(&sh.tempty[buf]));
             }
@@ -429,7 +491,11 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
                 tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) +
                                        (uint32_t)(buf * kBufCols + e * kStepKeys);
-                softmax_tile<G>(un, rs[pr], taddr, t, s2, s, sh, buf);
+                const int skey = un.k0 + t * kStepKeys;
+                if (t == 0 || skey + kStepKeys - 1 > sq.L - sq.ns)
+                    softmax_tile<G>(un, rs[pr], taddr, t, s2, s, sh, buf);
+                else
+                    softmax_tile_fast<G>(rs[pr], taddr, skey, t, sq.R, s2, sh, buf);
             }
         }
 #pragma unroll
