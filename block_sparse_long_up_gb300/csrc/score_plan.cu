@@ -136,12 +136,15 @@ __device__ __forceinline__ int find_seq_by_row(const SeqInfo *seqs, int B, int64
     return lo;
 }
 
-// Row statistics.  Per row r of a sequence: m_r = max_c mref[c][r] and
-// l_r = sum_c lsum[c][r] * 2^(mref[c][r] - m_r); writes m_r and 1/(l_r * n_s * Hq)
-// (the softmax normaliser and the query/head mean).  A CTA takes 32 consecutive
-// rows; its 8 warps take every 8th chunk slot and merge (max, sum) online, then
-// warp 0 merges the 8 partial results in warp order -- a fixed order, so the
-// result is bitwise reproducible.
+// Row statistics and chunk weights.  Per row r of a sequence:
+//     m_r = max_c mref[c][r],  l_r = sum_c lsum[c][r] * 2^(mref[c][r] - m_r),
+//     inv_r = 1 / (l_r * n_s * Hq)   (the softmax normaliser and the query/head mean)
+// and then, in place of mref[c][r], the weight of chunk c's partial sums:
+//     w[c][r] = 2^(mref[c][r] - m_r) * inv_r.
+// A CTA takes 32 consecutive rows; its 8 warps take every 8th chunk slot and
+// merge (max, sum) online, then warp 0 merges the 8 partial results in warp
+// order -- a fixed order, so the result is bitwise reproducible.  rowm/rowinv
+// keep m_r and inv_r.
 constexpr int kRowsPerCta = 32;
 constexpr int kSlotLanes = 8;
 
@@ -156,43 +159,63 @@ __device__ __forceinline__ void merge_ms(float &m, float &l, float mc, float lc)
 __global__ void __launch_bounds__(kRowsPerCta * kSlotLanes)
 finalize_rows_kernel(ScoreParams p) {
     __shared__ float sm[kSlotLanes][kRowsPerCta], sl[kSlotLanes][kRowsPerCta];
+    __shared__ float sM[kRowsPerCta], sI[kRowsPerCta];
     const int64_t total = p.counters->rows;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int64_t g0 = (int64_t)blockIdx.x * kRowsPerCta; g0 < total;
          g0 += (int64_t)gridDim.x * kRowsPerCta) {
         const int64_t gr = g0 + lane;
+        const bool ok = gr < total;
         float m = -INFINITY, l = 0.f;
-        if (gr < total) {
+        int nslots = 0, R = 0;
+        float *mr = nullptr;
+        const float *ls = nullptr;
+        if (ok) {
             const int s = find_seq_by_row(p.seqs, p.num_seqs, gr);
             const SeqInfo sq = p.seqs[s];
             const int64_t r = gr - sq.row_off;
-            const int nslots = sq.nchunks * kSlotsPerChunk;
-            const float *mr = p.mref + sq.stat_off + r;
-            const float *ls = p.lsum + sq.stat_off + r;
+            nslots = sq.nchunks * kSlotsPerChunk;
+            R = sq.R;
+            mr = p.mref + sq.stat_off + r;
+            ls = p.lsum + sq.stat_off + r;
+#pragma unroll 4
             for (int c = wid; c < nslots; c += kSlotLanes)
-                merge_ms(m, l, mr[(int64_t)c * sq.R], ls[(int64_t)c * sq.R]);
+                merge_ms(m, l, mr[(int64_t)c * R], ls[(int64_t)c * R]);
         }
         sm[wid][lane] = m;
         sl[wid][lane] = l;
         __syncthreads();
-        if (wid == 0 && gr < total) {
+        if (wid == 0) {
             float M = sm[0][lane], Lsum = sl[0][lane];
 #pragma unroll
             for (int w = 1; w < kSlotLanes; ++w) merge_ms(M, Lsum, sm[w][lane], sl[w][lane]);
-            const int s = find_seq_by_row(p.seqs, p.num_seqs, gr);
-            const float R = (float)p.seqs[s].R;
-            p.rowm[gr] = M;
-            p.rowinv[gr] = (M == -INFINITY || !(Lsum > 0.f)) ? 0.f : 1.0f / (Lsum * R);
+            const float inv = (M == -INFINITY || !(Lsum > 0.f)) ? 0.f : 1.0f / (Lsum * (float)R);
+            sM[lane] = M;
+            sI[lane] = inv;
+            if (ok) {
+                p.rowm[gr] = M;
+                p.rowinv[gr] = inv;
+            }
+        }
+        __syncthreads();
+        if (ok) {
+            const float M = sM[lane], inv = sI[lane];
+#pragma unroll 4
+            for (int c = wid; c < nslots; c += kSlotLanes) {
+                float *q = mr + (int64_t)c * R;
+                const float mc = *q;
+                *q = (mc == -INFINITY || inv == 0.f) ? 0.f : exp2f(mc - M) * inv;
+            }
         }
         __syncthreads();
     }
 }
 
 // Block scores.  A CTA takes one key chunk c of one sequence and up to 8 of its
-// blocks.  It first builds the chunk's row weights w[r] = 2^(mref[c][r] - m_r) * inv_r
-// in shared memory, then each warp reduces one block:
-//     score = sum_r part[b][r] * w[r]
-// lane i taking rows 4i.. (16-byte loads when the layout allows) into 4
+// blocks.  It stages the chunk's row weights w[c][r] in shared memory, then each
+// warp reduces one block:
+//     score = sum_r part[b][r] * w[c][r]
+// lane i taking float4 groups i, i+32, ... (eight loads in flight) into 4
 // interleaved accumulators, combined in a fixed order, then a fixed butterfly:
 // bitwise reproducible.
 constexpr int kBlocksPerCta = 8;
@@ -204,15 +227,13 @@ finalize_blocks_kernel(ScoreParams p) {
     if (p.counters->blocks <= 0) return;  // no valid plan (or nothing to do)
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int bpc = p.C / p.G;  // blocks per chunk
+    const int groups_per_chunk = (bpc + kBlocksPerCta - 1) / kBlocksPerCta;
     // CTA work item = (first block of a group of <= 8 blocks inside one chunk)
     for (int it = blockIdx.x;; it += gridDim.x) {
-        // map it -> global block: groups never straddle a chunk or a sequence
-        const int groups_per_chunk = (bpc + kBlocksPerCta - 1) / kBlocksPerCta;
-        // walk sequences until the group index falls inside one
+        // map it -> (sequence, chunk, group): groups never straddle a chunk or a sequence
         int rem = it, s = 0, found = 0;
         for (; s < p.num_seqs; ++s) {
-            const int nch = p.seqs[s].nchunks;
-            const int ng = nch * groups_per_chunk;
+            const int ng = p.seqs[s].nchunks * groups_per_chunk;
             if (rem < ng) { found = 1; break; }
             rem -= ng;
         }
@@ -222,53 +243,57 @@ finalize_blocks_kernel(ScoreParams p) {
         const int b_first = c * bpc + (rem % groups_per_chunk) * kBlocksPerCta;
         const int b_last = min(min(b_first + kBlocksPerCta, (c + 1) * bpc), sq.nb);
         if (b_first >= b_last) continue;  // a short last chunk has fewer blocks
-        const int slot = block_slot(b_first, p.G, p.C);
-        const float *mr = p.mref + sq.stat_off + (int64_t)slot * sq.R;
-        const float *rm = p.rowm + sq.row_off;
-        const float *ri = p.rowinv + sq.row_off;
+        const float *wr = p.mref + sq.stat_off + (int64_t)block_slot(b_first, p.G, p.C) * sq.R;
         const bool in_smem = sq.R <= kMaxRowsSmem;
+        const bool vec = (sq.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(wr) & 15) == 0) &&
+                         ((reinterpret_cast<uintptr_t>(p.part + sq.part_off) & 15) == 0);
         __syncthreads();
-        if (in_smem)
-            for (int r = threadIdx.x; r < sq.R; r += blockDim.x)
-                w[r] = exp2f(__ldg(mr + r) - __ldg(rm + r)) * __ldg(ri + r);
+        if (in_smem) {
+            if (vec) {
+                for (int i = threadIdx.x; i < sq.R / 4; i += blockDim.x)
+                    reinterpret_cast<float4 *>(w)[i] = __ldg(reinterpret_cast<const float4 *>(wr) + i);
+            } else {
+                for (int r = threadIdx.x; r < sq.R; r += blockDim.x) w[r] = __ldg(wr + r);
+            }
+        }
         __syncthreads();
         const int b = b_first + wid;
         if (b < b_last) {
             const float *pt = p.part + sq.part_off + (int64_t)b * sq.R;
+            const float *wv = in_smem ? w : wr;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            const bool vec = in_smem && (sq.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(pt) & 15) == 0);
             if (vec) {
                 const float4 *pt4 = reinterpret_cast<const float4 *>(pt);
-                const float4 *w4 = reinterpret_cast<const float4 *>(w);
+                const float4 *w4 = reinterpret_cast<const float4 *>(wv);
                 const int R4 = sq.R / 4;
                 int i = lane;
-                for (; i + 3 * 32 < R4; i += 4 * 32) {
-                    float4 x[4], y[4];
+                for (; i + 7 * 32 < R4; i += 8 * 32) {
+                    float4 x[8];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) x[k] = __ldcs(pt4 + i + k * 32);
+                    for (int k = 0; k < 8; ++k) x[k] = __ldcs(pt4 + i + k * 32);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) y[k] = w4[i + k * 32];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        acc[k] = fmaf(x[k].x, y[k].x, acc[k]);
-                        acc[k] = fmaf(x[k].y, y[k].y, acc[k]);
-                        acc[k] = fmaf(x[k].z, y[k].z, acc[k]);
-                        acc[k] = fmaf(x[k].w, y[k].w, acc[k]);
+                    for (int k = 0; k < 8; ++k) {
+                        const float4 y = w4[i + k * 32];
+                        float &a = acc[k & 3];
+                        a = fmaf(x[k].x, y.x, a);
+                        a = fmaf(x[k].y, y.y, a);
+                        a = fmaf(x[k].z, y.z, a);
+                        a = fmaf(x[k].w, y.w, a);
                     }
                 }
-                for (int k = 0; i < R4; i += 32, ++k) {
+                for (; i < R4; i += 32) {  // tail of fewer than 8 groups per lane
                     const float4 x = __ldcs(pt4 + i), y = w4[i];
-                    float &a = acc[k & 3];
-                    a = fmaf(x.x, y.x, a);
-                    a = fmaf(x.y, y.y, a);
-                    a = fmaf(x.z, y.z, a);
-                    a = fmaf(x.w, y.w, a);
+                    acc[0] = fmaf(x.x, y.x, acc[0]);
+                    acc[0] = fmaf(x.y, y.y, acc[0]);
+                    acc[0] = fmaf(x.z, y.z, acc[0]);
+                    acc[0] = fmaf(x.w, y.w, acc[0]);
                 }
             } else {
-                for (int r = lane, k = 0; r < sq.R; r += 32, ++k) {
-                    const float wr = in_smem ? w[r]
-                                             : exp2f(__ldg(mr + r) - __ldg(rm + r)) * __ldg(ri + r);
-                    acc[k & 3] = fmaf(__ldcs(pt + r), wr, acc[k & 3]);
+                for (int r = lane; r < sq.R; r += 4 * 32) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (r + k * 32 < sq.R)
+                            acc[k] = fmaf(__ldcs(pt + r + k * 32), wv[r + k * 32], acc[k]);
                 }
             }
             float t = (acc[0] + acc[1]) + (acc[2] + acc[3]);

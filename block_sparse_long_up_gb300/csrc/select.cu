@@ -7,12 +7,20 @@
 // block index.  The block at rank r is kept iff the mass ranked before it is
 // < p: that is exactly the shortest prefix whose cumulative mass reaches p
 // (crossing block included), and it keeps every block when the total falls
-// short of p.  Cumulative masses are exact sums of the fp32 scores in 64-bit
-// fixed point (2^-62 resolution), so they do not depend on summation order.
+// short of p.  Masses are the fp32 scores in 64-bit fixed point (score * 2^62,
+// truncated, by integer shifts of the float's fields), so every cumulative mass
+// is an exact integer sum that does not depend on summation order.
 //
-// The bitonic sort keeps E consecutive keys per thread in registers: exchanges
-// inside a thread use registers, exchanges inside a warp use shuffles, and only
-// exchanges across warps go through shared memory.
+// No sort is needed: the kept set is {key <= K*} for K*, the last key whose
+// mass-before is < P = ceil(p * 2^62).  K* is found by a radix search over the
+// key's digits, most significant first.  Each pass histograms the exact masses
+// (and counts) of the keys that share the digits found so far over the next
+// 8-bit digit (lanes of a warp holding the same digit combine their masses
+// first, so the shared-memory atomics stay few even when the leading digits
+// barely vary); the last non-empty bucket whose mass-before is < P holds K*
+// (the first key of that bucket is kept; the first key of any later bucket is
+// not).  A bucket holding a single key ends the search.  Six passes at most:
+// four over the 32 score bits, two over the block index (< 2^16).
 #include "../../include/up.h"
 #include "common.cuh"
 
@@ -20,145 +28,149 @@ namespace up {
 
 namespace {
 
-constexpr int kSelThreads = 1024;
-constexpr double kFix = 4611686018427387904.0;  // 2^62
+constexpr int kSelThreads = 512;
 
 __device__ __forceinline__ unsigned long long rank_key(float score, int idx) {
-    // scores are >= 0; -0 and anything not > 0 rank as 0
+    // scores are >= 0; -0, NaN and anything not > 0 rank as 0
     const unsigned bits = score > 0.f ? __float_as_uint(score) : 0u;
     return ((unsigned long long)(0xFFFFFFFFu - bits) << 32) | (unsigned)idx;
 }
 
-// score * 2^62, truncated (exact for scores >= 2^-38)
-__device__ __forceinline__ long long key_fixed(unsigned long long key) {
-    const float s = __uint_as_float(0xFFFFFFFFu - (unsigned)(key >> 32));
-    return (long long)((double)s * kFix);
-}
-
-// compare-exchange for element e against its partner's key b (partner index
-// e ^ j): the lower index of the pair keeps min for ascending runs (e & k == 0)
-__device__ __forceinline__ unsigned long long cx(unsigned long long a, unsigned long long b, int e,
-                                                 int j, int k) {
-    const bool lower = (e & j) == 0;
-    const bool asc = (e & k) == 0;
-    const unsigned long long mn = a < b ? a : b, mx = a < b ? b : a;
-    return (lower == asc) ? mn : mx;
+// score * 2^62 truncated, from the key's score bits; scores >= 1 count as 1.
+__device__ __forceinline__ unsigned long long key_fixed(unsigned long long key) {
+    const unsigned bits = 0xFFFFFFFFu - (unsigned)(key >> 32);
+    if (bits >= 0x3F800000u) return 1ull << 62;
+    const int e = (int)(bits >> 23);
+    if (e == 0) return 0ull;  // zero or subnormal (< 2^-126)
+    const unsigned long long m = (bits & 0x7FFFFFu) | 0x800000u;  // value = m * 2^(e-150)
+    const int sh = e - 88;                                       // times 2^62
+    return sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0ull);
 }
 
 template <int E>
-__device__ __forceinline__ void exchange_in_thread(unsigned long long (&v)[E], int t, int j, int k) {
+__device__ void select_one(const float *__restrict__ scores, int b0, int nb, int L, int G,
+                           unsigned long long P, bool keep_all, uint8_t *__restrict__ keep,
+                           int32_t *kept_tokens, int s) {
+    // bucket masses as four 16-bit pieces (each < 2^30 for <= 2^14 keys) and counts
+    __shared__ unsigned int hpart[4][256];
+    __shared__ unsigned int hcnt[256];
+    __shared__ unsigned long long s_prefix, s_base, s_kstar;
+    __shared__ unsigned int s_cnt;
+    __shared__ int shi[32];
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    // the rank key's high word per key; its low word is the index t + i * kSelThreads
+    unsigned khi[E];
 #pragma unroll
-    for (int jj = E / 2; jj >= 1; jj >>= 1) {
-        if (j == jj) {
+    for (int i = 0; i < E; ++i) {
+        const int e = t + i * kSelThreads;
+        khi[i] = e < nb ? (unsigned)(rank_key(scores[b0 + e], e) >> 32) : 0u;
+    }
+    auto key = [&](int i) {
+        return ((unsigned long long)khi[i] << 32) | (unsigned)(t + i * kSelThreads);
+    };
+    unsigned long long kstar = ~0ull;  // keep-all
+    if (!keep_all) {
+        unsigned long long prefix = 0ull, base = 0ull;
+        bool single = false;
+#pragma unroll 1
+        for (int ps = 0; ps < 6; ++ps) {
+            const int sh = ps < 4 ? 56 - 8 * ps : 40 - 8 * ps;  // 56, 48, 40, 32, 8, 0
+            if (t < 256) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) hpart[k][t] = 0u;
+                hcnt[t] = 0u;
+            }
+            __syncthreads();
 #pragma unroll
             for (int i = 0; i < E; ++i) {
-                if ((i & jj) == 0) {
-                    const int e = t * E + i;
-                    const bool asc = (e & k) == 0;
-                    const unsigned long long a = v[i], b = v[i + jj];
-                    const bool sw = (a > b) == asc;
-                    v[i] = sw ? b : a;
-                    v[i + jj] = sw ? a : b;
+                const int e = t + i * kSelThreads;
+                const bool match = ps == 0 || (key(i) >> (sh + 8)) == (prefix >> (sh + 8));
+                // 256 = not in the searched range; lanes with equal digits add
+                // their masses together and one of them updates the bucket
+                const unsigned dgt = (e < nb && match) ? (unsigned)((key(i) >> sh) & 255u) : 256u;
+                const unsigned peers = __match_any_sync(0xffffffffu, dgt);
+                const unsigned long long fx = dgt < 256u ? key_fixed(key(i)) : 0ull;
+                unsigned piece[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    piece[k] = __reduce_add_sync(peers, (unsigned)(fx >> (16 * k)) & 0xFFFFu);
+                if (dgt < 256u && lane == __ffs(peers) - 1) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) atomicAdd(&hpart[k][dgt], piece[k]);
+                    atomicAdd(&hcnt[dgt], (unsigned)__popc(peers));
                 }
             }
-        }
-    }
-}
-
-template <int E>
-__device__ void bitonic_sort(unsigned long long (&v)[E], int N, unsigned long long *sm) {
-    const int t = threadIdx.x;
-    for (int k = 2; k <= N; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            if (j >= 32 * E) {
+            __syncthreads();
+            if (wid == 0) {
+                // lane l owns buckets 8l .. 8l+7: exclusive scan of the lane totals
+                auto bucket_mass = [&](int bkt) {
+                    return (unsigned long long)hpart[0][bkt] +
+                           ((unsigned long long)hpart[1][bkt] << 16) +
+                           ((unsigned long long)hpart[2][bkt] << 32) +
+                           ((unsigned long long)hpart[3][bkt] << 48);
+                };
+                unsigned long long tot = 0ull;
 #pragma unroll
-                for (int i = 0; i < E; ++i) sm[t * E + i] = v[i];
-                __syncthreads();
+                for (int j = 0; j < 8; ++j) tot += bucket_mass(8 * lane + j);
+                unsigned long long x = tot;
 #pragma unroll
-                for (int i = 0; i < E; ++i) {
-                    const int e = t * E + i;
-                    v[i] = cx(v[i], sm[e ^ j], e, j, k);
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
                 }
-                __syncthreads();
-            } else if (j >= E) {
-                const int m = j / E;  // partner lane
+                unsigned long long S = base + (x - tot);  // mass before the lane's first bucket
+                int best = -1;
+                unsigned long long best_S = 0ull;
+                unsigned best_c = 0u;
 #pragma unroll
-                for (int i = 0; i < E; ++i) {
-                    const int e = t * E + i;
-                    v[i] = cx(v[i], __shfl_xor_sync(0xffffffffu, v[i], m), e, j, k);
+                for (int j = 0; j < 8; ++j) {
+                    const unsigned cj = hcnt[8 * lane + j];
+                    if (cj > 0u && S < P) {
+                        best = 8 * lane + j;
+                        best_S = S;
+                        best_c = cj;
+                    }
+                    S += bucket_mass(8 * lane + j);
                 }
-            } else {
-                exchange_in_thread<E>(v, t, j, k);
+                const int top = (int)__reduce_max_sync(0xffffffffu, (unsigned)(best + 1)) - 1;
+                if (best == top && best >= 0) {
+                    s_prefix = prefix | ((unsigned long long)best << sh);
+                    s_base = best_S;
+                    s_cnt = best_c;
+                }
             }
+            __syncthreads();
+            prefix = s_prefix;
+            base = s_base;
+            if (s_cnt == 1u) {  // the bucket's only key is K*
+#pragma unroll
+                for (int i = 0; i < E; ++i) {
+                    const int e = t + i * kSelThreads;
+                    if (e < nb && (key(i) >> sh) == (prefix >> sh)) s_kstar = key(i);
+                }
+                single = true;
+            }
+            __syncthreads();
+            if (single) break;
         }
+        kstar = single ? s_kstar : prefix;
     }
-}
-
-__device__ long long block_excl_scan_i64(long long v, long long *sh) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    long long x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) sh[wid] = x;
-    __syncthreads();
-    if (wid == 0) {
-        long long w = sh[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        sh[lane] = w;
-    }
-    __syncthreads();
-    const long long base = wid ? sh[wid - 1] : 0;
-    __syncthreads();
-    return base + (x - v);
-}
-
-template <int E>
-__device__ void select_one(const float *__restrict__ scores, int b0, int nb, int N, int L, int G,
-                           double p, uint8_t *__restrict__ keep, int32_t *kept_tokens, int s,
-                           unsigned long long *sm, long long *shl, int *shi) {
-    const int t = threadIdx.x;
-    unsigned long long v[E];
-#pragma unroll
-    for (int i = 0; i < E; ++i) {
-        const int e = t * E + i;
-        v[i] = e < nb ? rank_key(scores[b0 + e], e) : ~0ull;
-    }
-    bitonic_sort<E>(v, N, sm);
-    // thread t now holds ranks t*E .. t*E+E-1
-    long long fx[E], local = 0;
-#pragma unroll
-    for (int i = 0; i < E; ++i) {
-        fx[i] = (t * E + i < nb) ? key_fixed(v[i]) : 0;
-        local += fx[i];
-    }
-    long long before = block_excl_scan_i64(local, shl);
-    const bool all = !(p < 1.0);
-    const long long pfix = all ? 0 : (long long)ceil(p * kFix);
     int kept = 0;
 #pragma unroll
     for (int i = 0; i < E; ++i) {
-        const int r = t * E + i;
-        if (r < nb) {
-            const int idx = (int)(v[i] & 0xFFFFFFFFull);
-            const int k = (all || before < pfix) ? 1 : 0;
-            keep[b0 + idx] = (uint8_t)k;
-            if (k) kept += min(G, L - idx * G);
+        const int e = t + i * kSelThreads;
+        if (e < nb) {
+            const int k = key(i) <= kstar ? 1 : 0;
+            keep[b0 + e] = (uint8_t)k;
+            if (k) kept += min(G, L - e * G);
         }
-        before += fx[i];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) kept += __shfl_xor_sync(0xffffffffu, kept, o);
-    if ((t & 31) == 0) shi[t >> 5] = kept;
+    if (lane == 0) shi[wid] = kept;
     __syncthreads();
     if (t < 32) {
-        int w = shi[t];
+        int w = t < kSelThreads / 32 ? shi[t] : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
         if (t == 0) kept_tokens[s] = w;
@@ -167,11 +179,9 @@ __device__ void select_one(const float *__restrict__ scores, int b0, int nb, int
 
 __global__ void __launch_bounds__(kSelThreads)
 select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__ cu_blocks,
-                   const int32_t *__restrict__ cu, int G, double p, uint8_t *__restrict__ keep,
-                   int32_t *__restrict__ kept_tokens, unsigned int *err) {
-    extern __shared__ unsigned long long sm[];  // [UP_SELECT_MAX_BLOCKS]
-    __shared__ long long shl[32];
-    __shared__ int shi[32];
+                   const int32_t *__restrict__ cu, int G, unsigned long long P, int keep_all,
+                   uint8_t *__restrict__ keep, int32_t *__restrict__ kept_tokens,
+                   unsigned int *err) {
     const int s = blockIdx.x;
     const int b0 = cu_blocks[s];
     const int nb = cu_blocks[s + 1] - b0;
@@ -187,15 +197,13 @@ select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__
         }
         return;
     }
-    int N = kSelThreads;
-    while (N < nb) N <<= 1;
-    switch (N / kSelThreads) {
-        case 1: select_one<1>(scores, b0, nb, N, L, G, p, keep, kept_tokens, s, sm, shl, shi); break;
-        case 2: select_one<2>(scores, b0, nb, N, L, G, p, keep, kept_tokens, s, sm, shl, shi); break;
-        case 4: select_one<4>(scores, b0, nb, N, L, G, p, keep, kept_tokens, s, sm, shl, shi); break;
-        case 8: select_one<8>(scores, b0, nb, N, L, G, p, keep, kept_tokens, s, sm, shl, shi); break;
-        default: select_one<16>(scores, b0, nb, N, L, G, p, keep, kept_tokens, s, sm, shl, shi); break;
-    }
+    const bool all = keep_all != 0;
+    if (nb <= kSelThreads) select_one<1>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
+    else if (nb <= 2 * kSelThreads) select_one<2>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
+    else if (nb <= 4 * kSelThreads) select_one<4>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
+    else if (nb <= 8 * kSelThreads) select_one<8>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
+    else if (nb <= 16 * kSelThreads) select_one<16>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
+    else select_one<32>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
 }
 
 }  // namespace
@@ -203,13 +211,14 @@ select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__
 cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const int32_t *cu_seqlens,
                           int num_seqs, int G, double p, uint8_t *keep, int32_t *kept_tokens,
                           unsigned int *err, cudaStream_t st) {
-    const int smem = UP_SELECT_MAX_BLOCKS * (int)sizeof(unsigned long long);
-    cudaError_t e = cudaFuncSetAttribute(select_topp_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
     if (num_seqs <= 0) return cudaSuccess;
-    select_topp_kernel<<<num_seqs, kSelThreads, smem, st>>>(scores, cu_blocks, cu_seqlens, G, p,
-                                                             keep, kept_tokens, err);
+    static_assert(UP_SELECT_MAX_BLOCKS <= 32 * kSelThreads, "select keeps at most 32 keys per thread");
+    static_assert(UP_SELECT_MAX_BLOCKS <= 65536, "the radix search covers 16 index bits");
+    const bool all = !(p < 1.0);
+    // P = ceil(p * 2^62): p * 2^62 is exact in fp64, so this is the exact threshold
+    const unsigned long long P = all ? 0ull : (unsigned long long)ceil(p * 4611686018427387904.0);
+    select_topp_kernel<<<num_seqs, kSelThreads, 0, st>>>(scores, cu_blocks, cu_seqlens, G, P,
+                                                          all ? 1 : 0, keep, kept_tokens, err);
     return cudaGetLastError();
 }
 

@@ -111,12 +111,16 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
  * score are kept until their cumulative sum reaches p (e.g. 0.99).
  *
  * Per sequence, blocks are ranked by (score descending, block index
- * ascending); the cumulative score is taken in fp64 in rank order; the kept
- * set is the shortest prefix whose cumulative score is >= p, crossing block
- * included.  p >= 1 keeps every block; if rounding leaves the total below p,
- * every block is kept.
+ * ascending); the cumulative score is taken exactly in rank order (each fp32
+ * score as a 64-bit fixed-point multiple of 2^-62, truncated); the kept set is
+ * the shortest prefix whose cumulative score is >= p, crossing block included
+ * (block at rank r kept iff the mass ranked before it is < ceil(p * 2^62)).
+ * p >= 1 keeps every block; if rounding leaves the total below p, every block
+ * is kept.
  *
- *   scores, cu_blocks  as produced by up_score_blocks (scores >= 0).
+ *   scores, cu_blocks  as produced by up_score_blocks: block masses >= 0 that
+ *                      sum to about 1 per sequence (a score >= 1 counts as 1;
+ *                      a total above 2 gives an unspecified kept set).
  *   cu_seqlens         int32 [num_seqs+1] (block lengths for kept_tokens).
  *   p                  0 < p; p >= 1 keeps all.
  *   keep               uint8 [sum nb_s] (output): 1 kept, 0 dropped, original order.
