@@ -5,7 +5,39 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace up {
+
+// Programmatic dependent launch.  Every kernel of the library calls
+// pdl_trigger() first, so the next kernel of the stream may be scheduled while
+// this one still runs, and pdl_wait() before its first global-memory access:
+// that waits until the previous kernel of the stream has finished and its
+// writes are visible (read-after-write and write-after-read alike).  Work before
+// pdl_wait() touches only on-chip state (shared memory, barriers, TMEM) and
+// kernel parameters.  Both are no-ops for a kernel launched without the
+// attribute.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with programmatic stream serialization (see pdl_wait).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Per-sequence work description, written on the device by the plan kernel from
 // cu_seqlens, so the host never needs the sequence lengths.

@@ -45,6 +45,8 @@ __device__ int block_excl_scan_i32(int v, int *total, int *sh) {
 
 __global__ void __launch_bounds__(kIndexThreads)
 compact_index_kernel(CompactArgs a) {
+    pdl_trigger();
+    pdl_wait();
     int32_t *dst_blk = a.dst_blk;
     __shared__ int sh[32];
     const int B = a.num_seqs;
@@ -90,6 +92,8 @@ compact_index_kernel(CompactArgs a) {
 
 __global__ void __launch_bounds__(kGatherThreads)
 compact_gather_kernel(CompactArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const int K = *a.nkept;
     const int64_t items = (int64_t)K * a.items_per_block;
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
@@ -125,11 +129,9 @@ compact_gather_kernel(CompactArgs a) {
 }  // namespace
 
 cudaError_t launch_compact(const CompactArgs &a, int num_sms, cudaStream_t st) {
-    compact_index_kernel<<<1, kIndexThreads, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(compact_index_kernel, dim3(1), dim3(kIndexThreads), 0, st, a);
     if (e != cudaSuccess) return e;
-    compact_gather_kernel<<<num_sms * 4, kGatherThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(compact_gather_kernel, dim3(num_sms * 4), dim3(kGatherThreads), 0, st, a);
 }
 
 }  // namespace up

@@ -32,6 +32,8 @@ __device__ __forceinline__ void tile_logits(const __nv_bfloat16 *qT, const float
 template <int D>
 __global__ void __launch_bounds__(kRowsPerTile)
 score_fallback_kernel(ScoreParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int nflag = min(p.counters->flagged, p.flag_cap);
     extern __shared__ __align__(16) unsigned char smem[];
     __nv_bfloat16 *qT = reinterpret_cast<__nv_bfloat16 *>(smem);                 // [D][128]
@@ -117,8 +119,7 @@ cudaError_t launch_d(const ScoreParams &p, int num_sms, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(score_fallback_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    score_fallback_kernel<D><<<num_sms, kRowsPerTile, smem, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(score_fallback_kernel<D>, dim3(num_sms), dim3(kRowsPerTile), smem, st, p);
 }
 
 }  // namespace

@@ -55,6 +55,8 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
                   int64_t total_tokens, int Hq, int Hk, int d, int n, int G, int C,
                   unsigned int *err) {
     __shared__ int64_t sh[32];
+    pdl_trigger();
+    pdl_wait();
     const int g = Hq / Hk;
     // validate cu_seqlens
     int bad = 0;
@@ -160,6 +162,8 @@ __global__ void __launch_bounds__(kRowsPerCta * kSlotLanes)
 finalize_rows_kernel(ScoreParams p) {
     __shared__ float sm[kSlotLanes][kRowsPerCta], sl[kSlotLanes][kRowsPerCta];
     __shared__ float sM[kRowsPerCta], sI[kRowsPerCta];
+    pdl_trigger();
+    pdl_wait();
     const int64_t total = p.counters->rows;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int64_t g0 = (int64_t)blockIdx.x * kRowsPerCta; g0 < total;
@@ -211,96 +215,125 @@ finalize_rows_kernel(ScoreParams p) {
     }
 }
 
-// Block scores.  A CTA takes one key chunk c of one sequence and up to 8 of its
-// blocks.  It stages the chunk's row weights w[c][r] in shared memory, then each
-// warp reduces one block:
-//     score = sum_r part[b][r] * w[c][r]
-// lane i taking float4 groups i, i+32, ... (eight loads in flight) into 4
-// interleaved accumulators, combined in a fixed order, then a fixed butterfly:
-// bitwise reproducible.
-constexpr int kBlocksPerCta = 8;
-constexpr int kMaxRowsSmem = 8192;
+// Block scores.  score_b = sum_r part[b][r] * w[c(b)][r], with c(b) the chunk
+// of block b.  A CTA takes two blocks; four warps share a block, warp q taking
+// the q-th quarter of its rows as float4 groups (eight loads of part and eight
+// of w in flight per lane) into 4 interleaved accumulators, combined in a fixed
+// order, then a fixed butterfly, then the four quarters in order: bitwise
+// reproducible.
+constexpr int kBlocksPerCta = 2;
+constexpr int kWarpsPerBlock = 4;
 
-__global__ void __launch_bounds__(kBlocksPerCta * 32)
+// Ties 8 float4 values to this point of the program: every use of them comes
+// after it, so the loads that produce them are all issued before any use.
+__device__ __forceinline__ void hold8(float4 (&v)[8]) {
+    asm volatile(""
+                 : "+f"(v[0].x), "+f"(v[0].y), "+f"(v[0].z), "+f"(v[0].w), "+f"(v[1].x),
+                   "+f"(v[1].y), "+f"(v[1].z), "+f"(v[1].w), "+f"(v[2].x), "+f"(v[2].y),
+                   "+f"(v[2].z), "+f"(v[2].w), "+f"(v[3].x), "+f"(v[3].y), "+f"(v[3].z),
+                   "+f"(v[3].w), "+f"(v[4].x), "+f"(v[4].y), "+f"(v[4].z), "+f"(v[4].w),
+                   "+f"(v[5].x), "+f"(v[5].y), "+f"(v[5].z), "+f"(v[5].w), "+f"(v[6].x),
+                   "+f"(v[6].y), "+f"(v[6].z), "+f"(v[6].w), "+f"(v[7].x), "+f"(v[7].y),
+                   "+f"(v[7].z), "+f"(v[7].w));
+}
+
+// 16-byte loads issued in program order (so a batch is in flight together):
+// streaming (partials, read once) and read-only cached (weights).
+__device__ __forceinline__ float4 ld_stream4(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float4 ld_ro4(const float4 *p) {
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ int find_seq_by_block(const SeqInfo *seqs, int B, int gb) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (seqs[mid].blk_off <= gb) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kBlocksPerCta * kWarpsPerBlock * 32)
 finalize_blocks_kernel(ScoreParams p) {
-    __shared__ __align__(16) float w[kMaxRowsSmem];
-    if (p.counters->blocks <= 0) return;  // no valid plan (or nothing to do)
+    __shared__ float red[kBlocksPerCta][kWarpsPerBlock];
+    pdl_trigger();
+    pdl_wait();
+    const int nbt = p.counters->blocks;  // 0 when the plan is invalid
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int bpc = p.C / p.G;  // blocks per chunk
-    const int groups_per_chunk = (bpc + kBlocksPerCta - 1) / kBlocksPerCta;
-    // CTA work item = (first block of a group of <= 8 blocks inside one chunk)
-    for (int it = blockIdx.x;; it += gridDim.x) {
-        // map it -> (sequence, chunk, group): groups never straddle a chunk or a sequence
-        int rem = it, s = 0, found = 0;
-        for (; s < p.num_seqs; ++s) {
-            const int ng = p.seqs[s].nchunks * groups_per_chunk;
-            if (rem < ng) { found = 1; break; }
-            rem -= ng;
-        }
-        if (!found) break;
-        const SeqInfo sq = p.seqs[s];
-        const int c = rem / groups_per_chunk;
-        const int b_first = c * bpc + (rem % groups_per_chunk) * kBlocksPerCta;
-        const int b_last = min(min(b_first + kBlocksPerCta, (c + 1) * bpc), sq.nb);
-        if (b_first >= b_last) continue;  // a short last chunk has fewer blocks
-        const float *wr = p.mref + sq.stat_off + (int64_t)block_slot(b_first, p.G, p.C) * sq.R;
-        const bool in_smem = sq.R <= kMaxRowsSmem;
-        const bool vec = (sq.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(wr) & 15) == 0) &&
-                         ((reinterpret_cast<uintptr_t>(p.part + sq.part_off) & 15) == 0);
-        __syncthreads();
-        if (in_smem) {
-            if (vec) {
-                for (int i = threadIdx.x; i < sq.R / 4; i += blockDim.x)
-                    reinterpret_cast<float4 *>(w)[i] = __ldg(reinterpret_cast<const float4 *>(wr) + i);
-            } else {
-                for (int r = threadIdx.x; r < sq.R; r += blockDim.x) w[r] = __ldg(wr + r);
-            }
-        }
-        __syncthreads();
-        const int b = b_first + wid;
-        if (b < b_last) {
+    const int lb = wid / kWarpsPerBlock, q = wid % kWarpsPerBlock;
+    for (int g0 = blockIdx.x * kBlocksPerCta; g0 < nbt; g0 += gridDim.x * kBlocksPerCta) {
+        const int gb = g0 + lb;
+        float t = 0.f;
+        if (gb < nbt) {
+            const SeqInfo sq = p.seqs[find_seq_by_block(p.seqs, p.num_seqs, gb)];
+            const int b = gb - sq.blk_off;
+            const float *wr = p.mref + sq.stat_off + (int64_t)block_slot(b, p.G, p.C) * sq.R;
             const float *pt = p.part + sq.part_off + (int64_t)b * sq.R;
-            const float *wv = in_smem ? w : wr;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if (vec) {
+            if ((sq.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(wr) & 15) == 0) &&
+                ((reinterpret_cast<uintptr_t>(pt) & 15) == 0)) {
                 const float4 *pt4 = reinterpret_cast<const float4 *>(pt);
-                const float4 *w4 = reinterpret_cast<const float4 *>(wv);
+                const float4 *w4 = reinterpret_cast<const float4 *>(wr);
                 const int R4 = sq.R / 4;
-                int i = lane;
-                for (; i + 7 * 32 < R4; i += 8 * 32) {
-                    float4 x[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) x[k] = __ldcs(pt4 + i + k * 32);
+                const int per = (R4 + kWarpsPerBlock - 1) / kWarpsPerBlock;
+                const int lo = q * per, hi = min(lo + per, R4);
+                int i = lo + lane;
+                for (; i + 7 * 32 < hi; i += 8 * 32) {  // full batches: 16 loads in flight
+                    float4 x[8], y[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float4 y = w4[i + k * 32];
+                        x[k] = ld_stream4(pt4 + i + k * 32);
+                        y[k] = ld_ro4(w4 + i + k * 32);
+                    }
+                    hold8(x);
+                    hold8(y);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
                         float &a = acc[k & 3];
-                        a = fmaf(x[k].x, y.x, a);
-                        a = fmaf(x[k].y, y.y, a);
-                        a = fmaf(x[k].z, y.z, a);
-                        a = fmaf(x[k].w, y.w, a);
+                        a = fmaf(x[k].x, y[k].x, a);
+                        a = fmaf(x[k].y, y[k].y, a);
+                        a = fmaf(x[k].z, y[k].z, a);
+                        a = fmaf(x[k].w, y[k].w, a);
                     }
                 }
-                for (; i < R4; i += 32) {  // tail of fewer than 8 groups per lane
-                    const float4 x = __ldcs(pt4 + i), y = w4[i];
+                for (; i < hi; i += 32) {  // tail
+                    const float4 x = __ldcs(pt4 + i), y = __ldg(w4 + i);
                     acc[0] = fmaf(x.x, y.x, acc[0]);
                     acc[0] = fmaf(x.y, y.y, acc[0]);
                     acc[0] = fmaf(x.z, y.z, acc[0]);
                     acc[0] = fmaf(x.w, y.w, acc[0]);
                 }
             } else {
-                for (int r = lane; r < sq.R; r += 4 * 32) {
+                const int per = (sq.R + kWarpsPerBlock - 1) / kWarpsPerBlock;
+                const int lo = q * per, hi = min(lo + per, sq.R);
+                for (int r = lo + lane; r < hi; r += 4 * 32) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        if (r + k * 32 < sq.R)
-                            acc[k] = fmaf(__ldcs(pt + r + k * 32), wv[r + k * 32], acc[k]);
+                        if (r + k * 32 < hi)
+                            acc[k] = fmaf(__ldcs(pt + r + k * 32), __ldg(wr + r + k * 32), acc[k]);
                 }
             }
-            float t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-            if (lane == 0) p.scores[sq.blk_off + b] = t;
         }
+        if (lane == 0) red[lb][q] = t;
+        __syncthreads();
+        if (threadIdx.x < kBlocksPerCta && g0 + (int)threadIdx.x < nbt) {
+            const float *rq = red[threadIdx.x];
+            p.scores[g0 + threadIdx.x] = (rq[0] + rq[1]) + (rq[2] + rq[3]);
+        }
+        __syncthreads();
     }
 }
 
@@ -308,29 +341,25 @@ finalize_blocks_kernel(ScoreParams p) {
 
 cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, const ScoreParams &p,
                               int64_t total_tokens, cudaStream_t st) {
-    score_plan_kernel<<<1, kPlanThreads, 0, st>>>(
-        cu_seqlens, cu_blocks, const_cast<SeqInfo *>(p.seqs), const_cast<Counters *>(p.counters),
-        p.num_seqs, total_tokens, p.Hq, p.Hk, p.d, p.n, p.G, p.C, p.err);
-    return cudaGetLastError();
+    return launch_pdl(score_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, cu_seqlens, cu_blocks,
+                      const_cast<SeqInfo *>(p.seqs), const_cast<Counters *>(p.counters),
+                      p.num_seqs, total_tokens, p.Hq, p.Hk, p.d, p.n, p.G, p.C, p.err);
 }
 
 cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, cudaStream_t st) {
     if (lay.max_rows > 0) {
         const int64_t want = (lay.max_rows + kRowsPerCta - 1) / kRowsPerCta;
         const int grid = (int)(want < 65535 ? want : 65535);
-        finalize_rows_kernel<<<grid, kRowsPerCta * kSlotLanes, 0, st>>>(p);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(finalize_rows_kernel, dim3(grid), dim3(kRowsPerCta * kSlotLanes),
+                                   0, st, p);
         if (e != cudaSuccess) return e;
     }
     if (lay.max_blocks > 0) {
-        // one CTA per group of <= 8 blocks inside a chunk (extra CTAs exit at once)
-        const int64_t bpc = p.C / p.G;
-        const int64_t groups = (bpc + kBlocksPerCta - 1) / kBlocksPerCta;
-        const int64_t max_chunks = lay.total_tokens / p.C + p.num_seqs;
-        const int64_t want = groups * max_chunks;
+        // two blocks per CTA (CTAs past the real block count exit at once)
+        const int64_t want = (lay.max_blocks + kBlocksPerCta - 1) / kBlocksPerCta;
         const int grid = (int)(want < 65535 ? want : 65535);
-        finalize_blocks_kernel<<<grid, kBlocksPerCta * 32, 0, st>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(finalize_blocks_kernel, dim3(grid),
+                          dim3(kBlocksPerCta * kWarpsPerBlock * 32), 0, st, p);
     }
     return cudaSuccess;
 }

@@ -539,7 +539,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     uint8_t *qbuf = smem;                          // Q buffers (1024-aligned panels)
     uint8_t *kbuf = smem + C::kQBufs * C::kQBytes; // kStages x K panel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int units = p.counters->units;
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
@@ -570,6 +570,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
+    pdl_wait();  // the plan (and the kernels before it) are complete from here on
+    const int units = p.counters->units;
 
     if (warp == kWarpTmaK) {
         if (lane == 0) role_tma_k<D>(&kmap, p, sh, kbuf, units);
@@ -647,8 +649,8 @@ cudaError_t launch_dg(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
     if (e != cudaSuccess) return e;
     const int64_t grid = lay.max_units < num_sms ? lay.max_units : num_sms;
     if (grid < 1) return cudaSuccess;
-    score_tc_kernel<D, G><<<(unsigned)grid, kThreads, Cfg<D>::kSmem, st>>>(km, qm, p);
-    return cudaGetLastError();
+    return launch_pdl(score_tc_kernel<D, G>, dim3((unsigned)grid), dim3(kThreads), Cfg<D>::kSmem, st,
+                      km, qm, p);
 }
 
 template <int D>

@@ -182,6 +182,8 @@ select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__
                    const int32_t *__restrict__ cu, int G, unsigned long long P, int keep_all,
                    uint8_t *__restrict__ keep, int32_t *__restrict__ kept_tokens,
                    unsigned int *err) {
+    pdl_trigger();
+    pdl_wait();
     const int s = blockIdx.x;
     const int b0 = cu_blocks[s];
     const int nb = cu_blocks[s + 1] - b0;
@@ -217,9 +219,8 @@ cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const i
     const bool all = !(p < 1.0);
     // P = ceil(p * 2^62): p * 2^62 is exact in fp64, so this is the exact threshold
     const unsigned long long P = all ? 0ull : (unsigned long long)ceil(p * 4611686018427387904.0);
-    select_topp_kernel<<<num_seqs, kSelThreads, 0, st>>>(scores, cu_blocks, cu_seqlens, G, P,
-                                                          all ? 1 : 0, keep, kept_tokens, err);
-    return cudaGetLastError();
+    return launch_pdl(select_topp_kernel, dim3(num_seqs), dim3(kSelThreads), 0, st, scores,
+                      cu_blocks, cu_seqlens, G, P, all ? 1 : 0, keep, kept_tokens, err);
 }
 
 }  // namespace up
