@@ -309,12 +309,16 @@ def run_ours(args, inp, w, rank, world):
     kept = int(sp.total_kept.item())
     kept_blocks = int(sp.keep[: int(sp.cu_blocks[-1].item())].sum().item())
 
-    # timed region: K steps; per-call events on the launching stream, plus a pair
-    # recorded by the library around its tensor-core scoring kernel
+    # timed region: K steps, with only the pair of events the library records
+    # around its tensor-core scoring kernel (per-call events would sit between
+    # the kernels and cut their programmatic overlap; the per-call breakdown is
+    # taken in a separate loop below, outside the headline number)
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
-    for pair in ev:
-        for event in pair:
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    KB = min(K, 200)
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KB)]
+    for group in ev + evb:
+        for event in group:
             event.record(stream)  # creates the CUDA events before the timed region
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -328,16 +332,8 @@ def run_ours(args, inp, w, rank, world):
     clocks = ClockSampler(gpu_uuid)
     start.record(stream)
     for i in range(K):
-        e = ev[i]
-        e[0].record(stream)
-        up.set_kernel_timing_events(e[4], e[5])
-        up.score_blocks(q, k, cu, n, G, sp.scores, sp.cu_blocks, sp.ws_score)
-        e[1].record(stream)
-        up.select_topp(sp.scores, sp.cu_blocks, cu, G, p, sp.keep, sp.kept_tokens)
-        e[2].record(stream)
-        up.compact(x, pos, cu, G, sp.keep, sp.cu_blocks, sp.x_out, sp.pos_out, sp.cu_out,
-                   sp.src_idx, sp.total_kept, sp.ws_compact)
-        e[3].record(stream)
+        up.set_kernel_timing_events(ev[i][0], ev[i][1])
+        sp.run(q, k, cu, x, pos)
     end.record(stream)
     up.set_kernel_timing_events(None, None)
     torch.cuda.synchronize()
@@ -345,12 +341,25 @@ def run_ours(args, inp, w, rank, world):
     barrier(world)
     ms_total = start.elapsed_time(end)
     ms_step = max_over_ranks(ms_total / K, world)
-    t_score = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    t_select = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    t_compact = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
-    t_kernel = statistics.mean(e[4].elapsed_time(e[5]) for e in ev)
+    t_kernel = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     if up.get_device_error():
         raise RuntimeError("device error during the timed region")
+
+    # per-call breakdown (not part of the headline): events between the calls
+    for i in range(KB):
+        e = evb[i]
+        e[0].record(stream)
+        up.score_blocks(q, k, cu, n, G, sp.scores, sp.cu_blocks, sp.ws_score)
+        e[1].record(stream)
+        up.select_topp(sp.scores, sp.cu_blocks, cu, G, p, sp.keep, sp.kept_tokens)
+        e[2].record(stream)
+        up.compact(x, pos, cu, G, sp.keep, sp.cu_blocks, sp.x_out, sp.pos_out, sp.cu_out,
+                   sp.src_idx, sp.total_kept, sp.ws_compact)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    t_score = statistics.mean(e[0].elapsed_time(e[1]) for e in evb)
+    t_select = statistics.mean(e[1].elapsed_time(e[2]) for e in evb)
+    t_compact = statistics.mean(e[2].elapsed_time(e[3]) for e in evb)
 
     # end to end: host (pinned) inputs -> device, the three calls, result -> host
     E = args.e2e_steps

@@ -4,7 +4,7 @@
 // takes only the kept tokens; system-integration paragraph: the kept tokens'
 // positions travel with them.  A kept block is a contiguous run of at most G
 // rows, so compaction is a set of contiguous copies:
-//   index  (1 CTA)  exclusive scans over all blocks -> kept-block list
+//   index  (1 CTA)  one exclusive scan over per-thread block ranges -> kept-block list
 //                   (source row, destination row, rows), cu_seqlens_out, total;
 //   gather (persistent grid) one work item = up to rows_per_item rows of one
 //                   kept block, copied with 16-byte vector loads and stores.
@@ -17,76 +17,84 @@ namespace {
 constexpr int kIndexThreads = 1024;
 constexpr int kGatherThreads = 512;
 
-__device__ int block_excl_scan_i32(int v, int *total, int *sh) {
+// Block-wide exclusive scan of one int64 per thread (blockDim.x == 1024).
+__device__ int64_t block_excl_scan_i64(int64_t v, int64_t *total, int64_t *sh) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    int x = v;
+    int64_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) sh[wid] = x;
     __syncthreads();
     if (wid == 0) {
-        int w = sh[lane];
+        int64_t w = sh[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
         sh[lane] = w;
     }
     __syncthreads();
-    const int base = wid ? sh[wid - 1] : 0;
     *total = sh[31];
-    __syncthreads();
-    return base + x - v;
+    return (wid ? sh[wid - 1] : 0) + x - v;
 }
 
+// Thread t takes a contiguous range of blocks: it counts the kept rows and
+// blocks of its range, one block-wide scan of the (rows, blocks) pair gives its
+// starting destination row and list slot, and it writes its range.
 __global__ void __launch_bounds__(kIndexThreads)
 compact_index_kernel(CompactArgs a) {
     pdl_trigger();
     pdl_wait();
-    int32_t *dst_blk = a.dst_blk;
-    __shared__ int sh[32];
+    __shared__ int64_t sh[32];
     const int B = a.num_seqs;
-    const int total_blocks = a.cu_blocks[B];
-    int carry_rows = 0, carry_k = 0;
-    for (int t0 = 0; t0 < total_blocks; t0 += kIndexThreads) {
-        const int gb = t0 + threadIdx.x;
-        int len = 0, kf = 0, src = 0;
-        if (gb < total_blocks) {
-            int lo = 0, hi = B - 1;  // last sequence whose first block is <= gb
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (a.cu_blocks[mid] <= gb) lo = mid; else hi = mid - 1;
-            }
-            const int b = gb - a.cu_blocks[lo];
-            const int L = a.cu_seqlens[lo + 1] - a.cu_seqlens[lo];
-            src = a.cu_seqlens[lo] + b * a.G;
-            if (a.keep[gb]) {
-                len = min(a.G, L - b * a.G);
-                kf = 1;
-            }
+    const int nbt = a.cu_blocks[B];
+    const int per = (nbt + kIndexThreads - 1) / kIndexThreads;
+    const int g0 = min((int)threadIdx.x * per, nbt), g1 = min(g0 + per, nbt);
+    int s0 = 0;  // the sequence holding block g0 (the last one starting at or before it)
+    if (g0 < g1) {
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.cu_blocks[mid] <= g0) lo = mid; else hi = mid - 1;
         }
-        int tot_rows, tot_k;
-        const int er = block_excl_scan_i32(len, &tot_rows, sh);
-        const int ek = block_excl_scan_i32(kf, &tot_k, sh);
-        if (gb < total_blocks) {
-            dst_blk[gb] = carry_rows + er;
-            if (kf) a.list[carry_k + ek] = make_int4(src, carry_rows + er, len, 0);
-        }
-        carry_rows += tot_rows;
-        carry_k += tot_k;
+        s0 = lo;
     }
+    int rows = 0, kb = 0;
+    for (int gb = g0, s = s0; gb < g1; ++gb) {
+        while (a.cu_blocks[s + 1] <= gb) ++s;
+        if (a.keep[gb]) {
+            const int b = gb - a.cu_blocks[s];
+            rows += min(a.G, a.cu_seqlens[s + 1] - a.cu_seqlens[s] - b * a.G);
+            ++kb;
+        }
+    }
+    // rows in the high word, kept blocks in the low word (neither sum can carry)
+    int64_t tot;
+    const int64_t ex = block_excl_scan_i64(((int64_t)rows << 32) | kb, &tot, sh);
+    int dst = (int)(ex >> 32), slot = (int)(ex & 0xFFFFFFFF);
+    for (int gb = g0, s = s0; gb < g1; ++gb) {
+        while (a.cu_blocks[s + 1] <= gb) ++s;
+        a.dst_blk[gb] = dst;
+        if (a.keep[gb]) {
+            const int b = gb - a.cu_blocks[s];
+            const int len = min(a.G, a.cu_seqlens[s + 1] - a.cu_seqlens[s] - b * a.G);
+            a.list[slot++] = make_int4(a.cu_seqlens[s] + b * a.G, dst, len, 0);
+            dst += len;
+        }
+    }
+    const int total_rows = (int)(tot >> 32);
     __syncthreads();
     for (int s = threadIdx.x; s <= B; s += kIndexThreads) {
         const int cb = a.cu_blocks[s];
-        a.cu_out[s] = cb < total_blocks ? dst_blk[cb] : carry_rows;
+        a.cu_out[s] = cb < nbt ? a.dst_blk[cb] : total_rows;
     }
     if (threadIdx.x == 0) {
-        *a.total_kept = carry_rows;
-        *a.nkept = carry_k;
+        *a.total_kept = total_rows;
+        *a.nkept = (int)(tot & 0xFFFFFFFF);
     }
 }
 

@@ -1,7 +1,7 @@
 // score_plan.cu -- work planning and the deterministic finalize of block scoring.
 //
 // Scoring is split into three steps:
-//   plan      (1 CTA)  cu_seqlens -> per-sequence table, cu_blocks, work-unit count.
+//   plan      (1 warp) cu_seqlens -> per-sequence table, cu_blocks, work-unit count.
 //   main      (score kernel) per (row, block) partial softmax sums relative to a
 //             per (row, chunk) reference, plus the chunk's reference and sum.
 //             A work unit is (sequence, KV head, group of 128-row tiles, key chunk).
@@ -20,68 +20,55 @@ namespace up {
 
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 32;  // one warp: shuffle scans, no block barriers
 
-// Block-wide exclusive scan of one int64 per thread (blockDim.x == 1024).
-__device__ int64_t block_excl_scan(int64_t v, int64_t *total, int64_t *sh) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+// Warp-wide exclusive scan of one int64 per lane; *total = sum over the warp.
+__device__ __forceinline__ int64_t warp_excl_scan(int64_t v, int64_t *total) {
+    const int lane = threadIdx.x & 31;
     int64_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
-    if (lane == 31) sh[wid] = x;
-    __syncthreads();
-    if (wid == 0) {
-        int64_t w = sh[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int64_t y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        sh[lane] = w;  // inclusive prefix of warp totals
-    }
-    __syncthreads();
-    const int64_t warp_base = wid ? sh[wid - 1] : 0;
-    *total = sh[31];
-    __syncthreads();
-    return warp_base + x - v;
+    *total = __shfl_sync(0xffffffffu, x, 31);
+    return x - v;
 }
 
+// The plan: one warp walks the sequences 32 at a time (lane = sequence) and
+// carries the running offsets from one group to the next.
 __global__ void __launch_bounds__(kPlanThreads)
 score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_blocks,
                   SeqInfo *__restrict__ seqs, Counters *__restrict__ cnt, int B,
                   int64_t total_tokens, int Hq, int Hk, int d, int n, int G, int C,
                   unsigned int *err) {
-    __shared__ int64_t sh[32];
     pdl_trigger();
     pdl_wait();
+    const int lane = threadIdx.x;
     const int g = Hq / Hk;
     // validate cu_seqlens
     int bad = 0;
-    for (int s = threadIdx.x; s <= B; s += blockDim.x) {
+    for (int s = lane; s <= B; s += 32) {
         const int v = cu[s];
         if (s == 0 && v != 0) bad = 1;
         if (s > 0 && v < cu[s - 1]) bad = 1;
         if (s == B && (int64_t)v != total_tokens) bad = 1;
     }
-    bad = __syncthreads_or(bad);
-    if (bad) {
+    if (__any_sync(0xffffffffu, bad)) {
         // leave a well-formed empty plan: every later kernel sees no work
-        if (threadIdx.x == 0) {
+        if (lane == 0) {
             atomicOr(err, 0x1u);
             cnt->units = 0; cnt->blocks = 0; cnt->rows = 0; cnt->flagged = 0;
         }
-        for (int s = threadIdx.x; s <= B; s += blockDim.x) {
+        for (int s = lane; s <= B; s += 32) {
             cu_blocks[s] = 0;
             if (s < B) seqs[s] = SeqInfo{};
         }
         return;
     }
     int64_t base_q = 0, base_b = 0, base_u = 0, base_r = 0, base_p = 0, base_s = 0;
-    for (int t0 = 0; t0 < B; t0 += blockDim.x) {
-        const int s = t0 + threadIdx.x;
+    for (int t0 = 0; t0 < B; t0 += 32) {
+        const int s = t0 + lane;
         int64_t L = 0, ns = 0, nb = 0, nch = 0, mt = 0, R = 0, units = 0;
         if (s < B) {
             L = cu[s + 1] - cu[s];
@@ -94,12 +81,12 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
             units = (int64_t)Hk * mt * nch;
         }
         int64_t tq, tb, tu, tr, tp, ts;
-        const int64_t oq = block_excl_scan(ns, &tq, sh);
-        const int64_t ob = block_excl_scan(nb, &tb, sh);
-        const int64_t ou = block_excl_scan(units, &tu, sh);
-        const int64_t orow = block_excl_scan(R, &tr, sh);
-        const int64_t op = block_excl_scan(R * nb, &tp, sh);
-        const int64_t os = block_excl_scan(R * nch * kSlotsPerChunk, &ts, sh);
+        const int64_t oq = warp_excl_scan(ns, &tq);
+        const int64_t ob = warp_excl_scan(nb, &tb);
+        const int64_t ou = warp_excl_scan(units, &tu);
+        const int64_t orow = warp_excl_scan(R, &tr);
+        const int64_t op = warp_excl_scan(R * nb, &tp);
+        const int64_t os = warp_excl_scan(R * nch * kSlotsPerChunk, &ts);
         if (s < B) {
             SeqInfo si;
             si.tok_off = cu[s];
@@ -120,7 +107,7 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
         }
         base_q += tq; base_b += tb; base_u += tu; base_r += tr; base_p += tp; base_s += ts;
     }
-    if (threadIdx.x == 0) {
+    if (lane == 0) {
         cu_blocks[B] = (int32_t)base_b;
         cnt->units = (int32_t)base_u;
         cnt->blocks = (int32_t)base_b;
