@@ -72,6 +72,24 @@ def work_model(inp, G):
     return dict(flops=flops, exps=exps, score_bytes=score_bytes, blocks=nb)
 
 
+def step_roofline(wm, cbytes, tflops, hbm_gbs, ex2_rate, tokens, ms_step):
+    """Tokens/s of one step if every phase ran at its roof: scoring at the larger
+    of its tensor time and its K/Q/score HBM time, plus compaction at HBM speed
+    (the form the workload names), and the same with the exponential roof as a
+    third scoring term."""
+    t_mma = wm["flops"] / (tflops * 1e12)
+    t_bytes = wm["score_bytes"] / (hbm_gbs * 1e9)
+    t_exp = wm["exps"] / ex2_rate
+    t_cmp = cbytes / (hbm_gbs * 1e9)
+    roof = tokens / (max(t_mma, t_bytes) + t_cmp)
+    roof_exp = tokens / (max(t_mma, t_bytes, t_exp) + t_cmp)
+    value = tokens / (ms_step * 1e-3)
+    return dict(tokens_per_s=roof, frac=value / roof, tokens_per_s_with_exp=roof_exp,
+                frac_with_exp=value / roof_exp,
+                terms_us=dict(score_tensor=t_mma * 1e6, score_hbm=t_bytes * 1e6,
+                              score_exp=t_exp * 1e6, compact_hbm=t_cmp * 1e6))
+
+
 def compact_bytes(kept_tokens, hidden):
     # x rows read + written, positions read + written
     return kept_tokens * (2 * 2 * hidden + 8)
@@ -198,6 +216,22 @@ def oracle_sample(inp, heads, queries, threads, G, p):
     return dt, frac, hs, nq
 
 
+def cpu_model():
+    parts = {"0xd4f": "Arm Neoverse V2"}  # Arm's CPU part numbers
+    try:
+        for line in open("/proc/cpuinfo"):
+            key = line.split(":", 1)[0].strip().lower()
+            if key == "model name":
+                return line.split(":", 1)[1].strip()
+            if key == "cpu part":
+                part = line.split(":", 1)[1].strip()
+                return f"{parts.get(part, 'Arm')} (CPU part {part})"
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -308,6 +342,7 @@ def run_ours(args, inp, w, rank, world):
         raise RuntimeError("device error during warm-up")
     kept = int(sp.total_kept.item())
     kept_blocks = int(sp.keep[: int(sp.cu_blocks[-1].item())].sum().item())
+    ex2_rate = up.measure_ex2_rate()  # the exponential roof, measured on this GPU
 
     # timed region: K steps, with only the pair of events the library records
     # around its tensor-core scoring kernel (per-call events would sit between
@@ -405,6 +440,11 @@ def run_ours(args, inp, w, rank, world):
                       algorithmic_bytes=wm["score_bytes"],
                       peak_source=f"{peak_src} bf16 sustained (kernel timed inside a long loop)",
                       exp_rate_per_s=wm["exps"] / (t_kernel * 1e-3)),
+        exp_roof=dict(kernel="score_tc_kernel", achieved=wm["exps"] / (t_kernel * 1e-3),
+                      peak=ex2_rate, unit="exp/s", frac=wm["exps"] / (t_kernel * 1e-3) / ex2_rate,
+                      peak_source="measured in this run (up_measure_ex2_rate microbenchmark)"),
+        step_roofline=step_roofline(wm, cbytes, tc_peak, float(peaks["hbm_gbs"]), ex2_rate,
+                                    inp.total_tokens * world, ms_step),
         calls_ms=dict(score=t_score, score_kernel=t_kernel, select=t_select, compact=t_compact),
         compact_roofline=dict(bound="hbm", achieved=cbytes / (t_compact * 1e-3) / 1e9,
                               peak=float(peaks["hbm_gbs"]), unit="GB/s",
@@ -436,12 +476,12 @@ def main():
     out = run_ours(args, inp, w, rank, world)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            cores = cpu_cores()
-            threads = min(cores, 8)
-            dt, frac, hs, nq = oracle_sample(inp, 8, inp.n, threads, w["G"], w["p"])
+            # one query head per host core (the oracle's threads split the heads)
+            threads = max(1, min(cpu_cores(), inp.Hq))
+            dt, frac, hs, nq = oracle_sample(inp, threads, inp.n, threads, w["G"], w["p"])
             out["cpu_baseline"] = dict(
                 value=inp.total_tokens * frac / dt, unit=UNIT, cores=min(threads, hs),
-                kind="oracle",
+                kind="oracle", cpu=cpu_model(),
                 sample=f"{hs} of {inp.Hq} query heads x {nq} queries over all {inp.total_tokens} "
                        f"keys (fraction {frac:.4g} of the scoring work) plus top-p and "
                        f"compaction; tokens/s scaled to the full workload")

@@ -65,6 +65,8 @@ def lib():
     L.up_set_kernel_timing_events.restype = I
     L.up_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.up_get_device_error.restype = I
+    L.up_measure_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), P]
+    L.up_measure_ex2_rate.restype = I
     _lib = L
     return L
 
@@ -215,6 +217,14 @@ def set_kernel_timing_events(start=None, stop=None):
     of every later score_blocks call on this thread (None, None to stop)."""
     h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)
     _check("up_set_kernel_timing_events", lib().up_set_kernel_timing_events(h(start), h(stop)))
+
+
+def measure_ex2_rate(stream=None) -> float:
+    """The GPU's sustained MUFU ex2 rate in exponentials per second (a short
+    microbenchmark on the current device; synchronises the stream)."""
+    v = ctypes.c_double(0.0)
+    _check("up_measure_ex2_rate", lib().up_measure_ex2_rate(ctypes.byref(v), _stream(stream)))
+    return float(v.value)
 
 
 def get_device_error() -> int:

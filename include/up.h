@@ -208,6 +208,16 @@ typedef struct CUevent_st *up_event_t;
 up_status up_set_kernel_timing_events(up_event_t start_event, up_event_t stop_event);
 
 /*
+ * Instrumentation: measures this GPU's sustained MUFU ex2 rate (exponentials
+ * per second over the whole device) with a short full-occupancy kernel on
+ * `stream`, and writes it to *ex2_per_second.  Synchronises the stream (about
+ * a millisecond).  This is the exponential roof of up_score_blocks, which
+ * evaluates one ex2 per visible (query head, query, key) triple.  Not part of
+ * the method; no page counterpart.
+ */
+up_status up_measure_ex2_rate(double *ex2_per_second, up_stream_t stream);
+
+/*
  * Reads and clears the sticky device error word of the current device
  * (UP_DEVERR_* bits; 0 if none).  This call synchronises the device.
  * Returns UP_OK if no bit was set, UP_ERR_TIMEOUT if the timeout bit was set,

@@ -232,3 +232,11 @@ def test_overflowing_unit_takes_the_exact_fallback():
     nbad, worst = score_failures(g_sc, orc_sc)
     assert nbad == 0, (nbad, worst)
     assert up.get_device_error() == 0
+
+
+@pytest.mark.gpu
+def test_ex2_rate_probe():
+    """The exponential-roof microbenchmark returns a plausible device-wide rate
+    (a GB300 runs tens of ex2 per clock per SM on 152 SMs at ~2 GHz)."""
+    rate = up.measure_ex2_rate()
+    assert 1e11 < rate < 1e15
