@@ -90,20 +90,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
-// 16-byte global -> shared copy (Ampere-style cp.async); src_bytes = 0 writes zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- TMEM
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -146,10 +132,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // Same wait, with the loaded registers as in/out operands so that no use of
@@ -236,29 +218,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
-}
-
-// 2^x for two lanes on the FMA pipe (Cody-Waite range reduction + a degree-5
-// polynomial fitted to 2^f on [-1/2, 1/2] by iteratively reweighted least
-// squares on the relative error; max relative error ~2.4e-7 in fp32).
-// x is clamped at -127, so -inf gives ~2^-127 instead of 0.
-__device__ __forceinline__ uint64_t ex2_poly2(float x0, float x1) {
-    const uint64_t x = pack2(fmaxf(x0, -127.0f), fmaxf(x1, -127.0f));
-    const uint64_t t = add2(x, pack2(12582912.0f, 12582912.0f));      // 1.5*2^23: round to int
-    const uint64_t n = add2(t, pack2(-12582912.0f, -12582912.0f));
-    const uint64_t f = fma2(n, pack2(-1.0f, -1.0f), x);               // f = x - n in [-1/2, 1/2]
-    uint64_t q = fma2(pack2(1.3276379e-3f, 1.3276379e-3f), f, pack2(9.6755102e-3f, 9.6755102e-3f));
-    q = fma2(q, f, pack2(5.5507131e-2f, 5.5507131e-2f));
-    q = fma2(q, f, pack2(2.4022120e-1f, 2.4022120e-1f));
-    q = fma2(q, f, pack2(6.9314694e-1f, 6.9314694e-1f));
-    q = fma2(q, f, pack2(1.0000001f, 1.0000001f));
-    float q0, q1, t0, t1;
-    unpack2(q, q0, q1);
-    unpack2(t, t0, t1);
-    // scale by 2^n: the integer n sits in the low mantissa bits of t
-    const float r0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
-    const float r1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
-    return pack2(r0, r1);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
