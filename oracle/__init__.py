@@ -52,6 +52,10 @@ def _load():
             lib.orc_block_scores.restype = i32
             lib.orc_select_topp.argtypes = [P, P, P, i32, i32, dbl, P, P, P, P]
             lib.orc_select_topp.restype = i32
+            lib.orc_select_topk.argtypes = [P, P, P, i32, i32, i32, P, P]
+            lib.orc_select_topk.restype = i32
+            lib.orc_keep_last_block.argtypes = [P, P, i32, i32, P, P]
+            lib.orc_keep_last_block.restype = i32
             lib.orc_compact.argtypes = [P, P, i64, P, i32, i32, P, P, P, P, P, P]
             lib.orc_compact.restype = i64
             _lib = lib
@@ -123,6 +127,34 @@ def select_topp(scores, cu_blocks, cu_seqlens, G, p):
     if rc != 0:
         raise ValueError("orc_select_topp rejected its arguments")
     return keep, kept, ci, ce
+
+
+def select_topk(scores, cu_blocks, cu_seqlens, G, k):
+    """Top-k selection.  Returns (keep uint8, kept_tokens int32)."""
+    lib = _load()
+    scores = _c(scores, np.float64)
+    cb = _c(cu_blocks, np.int32)
+    cu = _c(cu_seqlens, np.int32)
+    B = cu.shape[0] - 1
+    keep = np.zeros(scores.shape[0], dtype=np.uint8)
+    kept = np.zeros(B, dtype=np.int32)
+    rc = lib.orc_select_topk(_ptr(scores), _ptr(cb), _ptr(cu), B, G, int(k), _ptr(keep), _ptr(kept))
+    if rc != 0:
+        raise ValueError("orc_select_topk rejected its arguments")
+    return keep, kept
+
+
+def keep_last_block(keep, kept_tokens, cu_blocks, cu_seqlens, G):
+    """The keep-last option applied to a selection.  Returns new (keep, kept_tokens)."""
+    lib = _load()
+    keep = np.array(keep, dtype=np.uint8, copy=True)
+    kept = np.array(kept_tokens, dtype=np.int32, copy=True)
+    cb = _c(cu_blocks, np.int32)
+    cu = _c(cu_seqlens, np.int32)
+    rc = lib.orc_keep_last_block(_ptr(cb), _ptr(cu), cu.shape[0] - 1, G, _ptr(keep), _ptr(kept))
+    if rc != 0:
+        raise ValueError("orc_keep_last_block rejected its arguments")
+    return keep, kept
 
 
 def compact(x, pos, cu_seqlens, G, keep, cu_blocks, with_x=True):

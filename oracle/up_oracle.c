@@ -31,13 +31,16 @@
  *   - top-p keeps the minimal score-sorted prefix whose cumulative mass reaches
  *     p, including the crossing block; p >= 1 keeps every block; ties go to the
  *     lower block index; cumulative sums are fp64;
+ *   - top-k keeps the first min(k, nb) blocks of the same ranking; the
+ *     optional keep-last step also keeps each sequence's last block;
  *   - compaction keeps ascending original order; positions are gathered, not
  *     renumbered.
  *
  * Pins (tests/test_oracle_pins.py): closed form for q == 0, a hand-worked
  * two-key softmax, fp64 torch.softmax on dense tiny cases, sum-to-one, the
  * G = 1 and G >= L special cases, GQA == MHA with repeated KV heads,
- * hand-enumerated and brute-force top-p sets, and compaction invariants.
+ * hand-enumerated and brute-force top-p and top-k sets, the keep-last step,
+ * and compaction invariants.
  */
 #include <math.h>
 #include <pthread.h>
@@ -236,6 +239,63 @@ int orc_select_topp(const double *scores, const int32_t *cu_blocks, const int32_
             kept_tokens[s] += end - b * G;
         }
         free(order);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Top-k selection.  [UP] hyper-parameters paragraph: the ablation sets top-p  */
+/* against keeping a fixed number of blocks per sequence (top-k).  Blocks are */
+/* ranked exactly as for top-p (score descending, ties to the lower index)    */
+/* and the first min(k, nb) ranks are kept.  Returns 0, or -1 on bad args.    */
+/* ------------------------------------------------------------------------ */
+int orc_select_topk(const double *scores, const int32_t *cu_blocks, const int32_t *cu_seqlens,
+                    int num_seqs, int G, int k, uint8_t *keep, int32_t *kept_tokens)
+{
+    if (G < 1 || num_seqs < 0 || k < 1) return -1;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int nb = cu_blocks[s + 1] - cu_blocks[s];
+        const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+        const double *sc = scores + cu_blocks[s];
+        kept_tokens[s] = 0;
+        if (nb == 0) continue;
+        int *order = (int *)malloc(sizeof(int) * (size_t)nb);
+        if (!order) return -1;
+        for (int b = 0; b < nb; ++b) order[b] = b;
+        orc_sort_scores = sc;
+        qsort(order, (size_t)nb, sizeof(int), orc_rank_cmp);
+        for (int b = 0; b < nb; ++b) keep[cu_blocks[s] + b] = 0;
+        for (int r = 0; r < nb && r < k; ++r) {
+            const int b = order[r];
+            const int end = (b + 1) * G < L ? (b + 1) * G : L;
+            keep[cu_blocks[s] + b] = 1;
+            kept_tokens[s] += end - b * G;
+        }
+        free(order);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Keep-last option.  [UP] system-integration paragraph: decode continues     */
+/* from the end of each sequence.  As an option applied after either          */
+/* selection, the last block of every non-empty sequence (its most recent     */
+/* tokens) is also kept and kept_tokens counts it; the method as the pages    */
+/* state it leaves this off.  Returns 0, or -1 on bad args.                   */
+/* ------------------------------------------------------------------------ */
+int orc_keep_last_block(const int32_t *cu_blocks, const int32_t *cu_seqlens, int num_seqs,
+                        int G, uint8_t *keep, int32_t *kept_tokens)
+{
+    if (G < 1 || num_seqs < 0) return -1;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int nb = cu_blocks[s + 1] - cu_blocks[s];
+        const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+        if (nb == 0) continue;
+        const int b = nb - 1;
+        if (!keep[cu_blocks[s] + b]) {
+            keep[cu_blocks[s] + b] = 1;
+            kept_tokens[s] += L - b * G;
+        }
     }
     return 0;
 }

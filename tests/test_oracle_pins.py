@@ -285,6 +285,84 @@ def test_topp_cumulative_band_outputs():
 
 
 # --------------------------------------------------------------------------
+# top-k selection and the keep-last option
+# --------------------------------------------------------------------------
+
+def _load_topk_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "topk_hand_enumerated.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, scores, kept = (part.strip() for part in line.split(";"))
+            cases.append((int(k), [float(v) for v in scores.split(",")],
+                          sorted(int(v) for v in kept.split(","))))
+    return cases
+
+
+@pytest.mark.parametrize("k,scores,kept", _load_topk_golden())
+def test_topk_hand_enumerated(k, scores, kept):
+    nb, G = len(scores), 4
+    keep, kt = oracle.select_topk(np.array(scores), np.array([0, nb], np.int32),
+                                  np.array([0, nb * G], np.int32), G, k)
+    assert sorted(np.nonzero(keep)[0].tolist()) == kept
+    assert kt.tolist() == [len(kept) * G]
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_topk_brute_force(seed):
+    """For nb <= 12, with scores drawn from a few values (many ties): the kept set
+    is the lexicographically smallest (sorted indices) among the k-subsets of
+    largest total score, which is what ranking with ties to the lower index picks."""
+    rng = np.random.default_rng(300 + seed)
+    nb = int(rng.integers(1, 13))
+    scores = rng.choice(np.array([0.5, 0.25, 0.125, 0.0625]), size=nb)
+    k = int(rng.integers(1, nb + 3))
+    G = 8
+    L = nb * G - int(rng.integers(0, G))
+    keep, kt = oracle.select_topk(scores, np.array([0, nb], np.int32),
+                                  np.array([0, L], np.int32), G, k)
+    m = min(k, nb)
+    best = max(scores[list(c)].sum() for c in itertools.combinations(range(nb), m))
+    cands = [c for c in itertools.combinations(range(nb), m) if scores[list(c)].sum() == best]
+    assert tuple(np.nonzero(keep)[0].tolist()) == min(cands)
+    lens = [min(G, L - b * G) for b in range(nb)]
+    assert kt[0] == sum(lens[b] for b in np.nonzero(keep)[0])
+
+
+def test_topk_zero_queries_keeps_lowest_indices():
+    """q == 0: equal scores before the query window, lower inside it; top-k keeps
+    the first k block indices (the tie rule at scale)."""
+    L, n, G, Hq, Hk, d = 1024, 64, 16, 2, 1, 8
+    _, k, cu = _random_case([L], Hq, Hk, d, n, seed=2)
+    q = np.zeros((n, Hq, d), np.uint16)
+    sc, cb = oracle.score_blocks(q, k, cu, Hq, Hk, d, n, G)
+    for kk in (1, 7, 30):
+        keep, _ = oracle.select_topk(sc, cb, cu, G, kk)
+        assert np.nonzero(keep)[0].tolist() == list(range(kk))
+
+
+def test_keep_last_block_option():
+    """The keep-last step keeps each non-empty sequence's last block (ragged length
+    counted) and leaves a selection that already holds it unchanged."""
+    lens = [37, 64, 0, 5]
+    G = 16
+    cu = np.array([0] + list(np.cumsum(lens)), np.int32)
+    nbs = [(L + G - 1) // G for L in lens]
+    cb = np.array([0] + list(np.cumsum(nbs)), np.int32)
+    keep = np.zeros(int(cb[-1]), np.uint8)
+    keep[0] = 1                    # sequence 0: first block only
+    keep[int(cb[1]) + 3] = 1       # sequence 1: already holds its last block
+    kept = np.array([16, 16, 0, 0], np.int32)
+    k2, t2 = oracle.keep_last_block(keep, kept, cb, cu, G)
+    assert k2[int(cb[1]) - 1] == 1 and t2[0] == 16 + (37 - 2 * 16)
+    assert t2[1] == 16 and k2[int(cb[1]):int(cb[2])].tolist() == [0, 0, 0, 1]
+    assert t2[2] == 0
+    assert k2[int(cb[3])] == 1 and t2[3] == 5
+
+
+# --------------------------------------------------------------------------
 # compaction
 # --------------------------------------------------------------------------
 
