@@ -351,7 +351,7 @@ def run_ours(args, inp, w, rank, world):
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     KB = min(K, 200)
-    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KB)]
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(KB)]
     for group in ev + evb:
         for event in group:
             event.record(stream)  # creates the CUDA events before the timed region
@@ -381,6 +381,8 @@ def run_ours(args, inp, w, rank, world):
         raise RuntimeError("device error during the timed region")
 
     # per-call breakdown (not part of the headline): events between the calls
+    keep_k = torch.empty_like(sp.keep)
+    kt_k = torch.empty_like(sp.kept_tokens)
     for i in range(KB):
         e = evb[i]
         e[0].record(stream)
@@ -391,10 +393,15 @@ def run_ours(args, inp, w, rank, world):
         up.compact(x, pos, cu, G, sp.keep, sp.cu_blocks, sp.x_out, sp.pos_out, sp.cu_out,
                    sp.src_idx, sp.total_kept, sp.ws_compact)
         e[3].record(stream)
+        # the top-k rule (same ranking) at the block count top-p kept, into scratch flags
+        up.select_blocks(sp.scores, sp.cu_blocks, cu, G, mode="top_k", k=max(1, kept_blocks),
+                         keep=keep_k, kept_tokens=kt_k)
+        e[4].record(stream)
     torch.cuda.synchronize()
     t_score = statistics.mean(e[0].elapsed_time(e[1]) for e in evb)
     t_select = statistics.mean(e[1].elapsed_time(e[2]) for e in evb)
     t_compact = statistics.mean(e[2].elapsed_time(e[3]) for e in evb)
+    t_select_k = statistics.mean(e[3].elapsed_time(e[4]) for e in evb)
 
     # end to end: host (pinned) inputs -> device, the three calls, result -> host
     E = args.e2e_steps
@@ -445,7 +452,8 @@ def run_ours(args, inp, w, rank, world):
                       peak_source="measured in this run (up_measure_ex2_rate microbenchmark)"),
         step_roofline=step_roofline(wm, cbytes, tc_peak, float(peaks["hbm_gbs"]), ex2_rate,
                                     inp.total_tokens * world, ms_step),
-        calls_ms=dict(score=t_score, score_kernel=t_kernel, select=t_select, compact=t_compact),
+        calls_ms=dict(score=t_score, score_kernel=t_kernel, select=t_select, compact=t_compact,
+                      select_topk=t_select_k),
         compact_roofline=dict(bound="hbm", achieved=cbytes / (t_compact * 1e-3) / 1e9,
                               peak=float(peaks["hbm_gbs"]), unit="GB/s",
                               frac=cbytes / (t_compact * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),

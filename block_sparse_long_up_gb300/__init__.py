@@ -55,6 +55,8 @@ def lib():
     L.up_score_blocks.restype = I
     L.up_select_topp.argtypes = [P, P, P, I, I, ctypes.c_double, P, P, P]
     L.up_select_topp.restype = I
+    L.up_select_blocks.argtypes = [P, P, P, I, I, I, ctypes.c_double, I, ctypes.c_uint32, P, P, P]
+    L.up_select_blocks.restype = I
     L.up_compact_workspace.argtypes = [I, I64, I]
     L.up_compact_workspace.restype = SZ
     L.up_compact.argtypes = [P, P, I, P, I, I64, I, P, P, P, P, P, P, P, P, SZ, P]
@@ -152,6 +154,36 @@ def select_topp(scores, cu_blocks, cu_seqlens, G, p, keep=None, kept_tokens=None
     st = lib().up_select_topp(_ptr(scores), _ptr(cu_blocks), _ptr(cu_seqlens), B, G, float(p),
                               _ptr(keep), _ptr(kept_tokens), _stream(stream))
     _check("up_select_topp", st)
+    return keep, kept_tokens
+
+
+SELECT_MODES = {"top_p": 0, "top_k": 1}
+SELECT_KEEP_LAST = 0x1
+
+
+def select_blocks(scores, cu_blocks, cu_seqlens, G, mode="top_p", p=0.99, k=1, keep_last=False,
+                  keep=None, kept_tokens=None, stream=None):
+    """Block selection, general form: mode "top_p" (threshold p) or "top_k" (the
+    first k ranks), optionally also keeping each sequence's last block.  Returns
+    (keep uint8 [sum nb_s], kept_tokens int32 [B])."""
+    if mode not in SELECT_MODES:
+        raise ValueError(f"mode must be one of {sorted(SELECT_MODES)}")
+    _need(scores, "scores", torch.float32)
+    dev = scores.device
+    _need(cu_blocks, "cu_blocks", torch.int32, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    B = cu_seqlens.numel() - 1
+    if keep is None:
+        keep = torch.empty(max(scores.numel(), 1), dtype=torch.uint8, device=dev)
+    if kept_tokens is None:
+        kept_tokens = torch.empty(max(B, 1), dtype=torch.int32, device=dev)
+    _need(keep, "keep", torch.uint8, dev)
+    _need(kept_tokens, "kept_tokens", torch.int32, dev)
+    flags = SELECT_KEEP_LAST if keep_last else 0
+    st = lib().up_select_blocks(_ptr(scores), _ptr(cu_blocks), _ptr(cu_seqlens), B, G,
+                                SELECT_MODES[mode], float(p), int(k), flags, _ptr(keep),
+                                _ptr(kept_tokens), _stream(stream))
+    _check("up_select_blocks", st)
     return keep, kept_tokens
 
 

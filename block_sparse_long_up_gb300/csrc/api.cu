@@ -241,8 +241,34 @@ up_status up_select_topp(const float *scores, const int32_t *cu_blocks,
     DeviceState *ds = nullptr;
     up_status st = device_state(&ds);
     if (st != UP_OK) return st;
-    if (up::launch_select(scores, cu_blocks, cu_seqlens, num_seqs, G, p, keep, kept_tokens,
-                          ds->err, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (up::launch_select(scores, cu_blocks, cu_seqlens, num_seqs, G, false, p, 0, false, keep,
+                          kept_tokens, ds->err, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return UP_ERR_CUDA;
+    return UP_OK;
+}
+
+up_status up_select_blocks(const float *scores, const int32_t *cu_blocks,
+                           const int32_t *cu_seqlens, int num_seqs, int G, up_select_mode mode,
+                           double p, int k, uint32_t flags, uint8_t *keep, int32_t *kept_tokens,
+                           up_stream_t stream) {
+    if (num_seqs < 0 || G < 1 || (flags & ~UP_SELECT_KEEP_LAST) != 0) return UP_ERR_INVALID_ARG;
+    if (mode == UP_SELECT_TOP_P) {
+        if (!(p > 0.0)) return UP_ERR_INVALID_ARG;
+    } else if (mode == UP_SELECT_TOP_K) {
+        if (k < 1) return UP_ERR_INVALID_ARG;
+    } else {
+        return UP_ERR_INVALID_ARG;
+    }
+    if (!valid_G(G)) return UP_ERR_UNSUPPORTED;
+    if (num_seqs > 0 && (!scores || !cu_blocks || !cu_seqlens || !keep || !kept_tokens))
+        return UP_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    up_status st = device_state(&ds);
+    if (st != UP_OK) return st;
+    if (up::launch_select(scores, cu_blocks, cu_seqlens, num_seqs, G, mode == UP_SELECT_TOP_K, p,
+                          k, (flags & UP_SELECT_KEEP_LAST) != 0, keep, kept_tokens, ds->err,
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return UP_ERR_CUDA;
     return UP_OK;
 }

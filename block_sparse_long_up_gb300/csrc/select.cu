@@ -11,8 +11,13 @@
 // truncated, by integer shifts of the float's fields), so every cumulative mass
 // is an exact integer sum that does not depend on summation order.
 //
+// Top-k (UniPrefill overview, hyper-parameters paragraph: the ablation against
+// a fixed number of kept blocks) is the same search with every key's mass set
+// to 1 and P = k: the block at rank r is kept iff r < k.  The keep-last option
+// (after either rule) also keeps each sequence's last block.
+//
 // No sort is needed: the kept set is {key <= K*} for K*, the last key whose
-// mass-before is < P = ceil(p * 2^62).  K* is found by a radix search over the
+// mass-before is < P (top-p: P = ceil(p * 2^62)).  K* is found by a radix search over the
 // key's digits, most significant first.  Each pass histograms the exact masses
 // (and counts) of the keys that share the digits found so far over the next
 // 8-bit digit (lanes of a warp holding the same digit combine their masses
@@ -49,8 +54,8 @@ __device__ __forceinline__ unsigned long long key_fixed(unsigned long long key) 
 
 template <int E>
 __device__ void select_one(const float *__restrict__ scores, int b0, int nb, int L, int G,
-                           unsigned long long P, bool keep_all, uint8_t *__restrict__ keep,
-                           int32_t *kept_tokens, int s) {
+                           unsigned long long P, bool unit_mass, bool keep_all, bool keep_last,
+                           uint8_t *__restrict__ keep, int32_t *kept_tokens, int s) {
     // bucket masses as four 16-bit pieces (each < 2^30 for <= 2^14 keys) and counts
     __shared__ unsigned int hpart[4][256];
     __shared__ unsigned int hcnt[256];
@@ -89,7 +94,8 @@ __device__ void select_one(const float *__restrict__ scores, int b0, int nb, int
                 // their masses together and one of them updates the bucket
                 const unsigned dgt = (e < nb && match) ? (unsigned)((key(i) >> sh) & 255u) : 256u;
                 const unsigned peers = __match_any_sync(0xffffffffu, dgt);
-                const unsigned long long fx = dgt < 256u ? key_fixed(key(i)) : 0ull;
+                const unsigned long long fx =
+                    dgt < 256u ? (unit_mass ? 1ull : key_fixed(key(i))) : 0ull;
                 unsigned piece[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
@@ -160,7 +166,7 @@ __device__ void select_one(const float *__restrict__ scores, int b0, int nb, int
     for (int i = 0; i < E; ++i) {
         const int e = t + i * kSelThreads;
         if (e < nb) {
-            const int k = key(i) <= kstar ? 1 : 0;
+            const int k = (key(i) <= kstar || (keep_last && e == nb - 1)) ? 1 : 0;
             keep[b0 + e] = (uint8_t)k;
             if (k) kept += min(G, L - e * G);
         }
@@ -179,9 +185,9 @@ __device__ void select_one(const float *__restrict__ scores, int b0, int nb, int
 
 __global__ void __launch_bounds__(kSelThreads)
 select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__ cu_blocks,
-                   const int32_t *__restrict__ cu, int G, unsigned long long P, int keep_all,
-                   uint8_t *__restrict__ keep, int32_t *__restrict__ kept_tokens,
-                   unsigned int *err) {
+                   const int32_t *__restrict__ cu, int G, unsigned long long P, int unit_mass,
+                   int keep_all, int keep_last, uint8_t *__restrict__ keep,
+                   int32_t *__restrict__ kept_tokens, unsigned int *err) {
     pdl_trigger();
     pdl_wait();
     const int s = blockIdx.x;
@@ -199,28 +205,36 @@ select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__
         }
         return;
     }
-    const bool all = keep_all != 0;
-    if (nb <= kSelThreads) select_one<1>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
-    else if (nb <= 2 * kSelThreads) select_one<2>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
-    else if (nb <= 4 * kSelThreads) select_one<4>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
-    else if (nb <= 8 * kSelThreads) select_one<8>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
-    else if (nb <= 16 * kSelThreads) select_one<16>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
-    else select_one<32>(scores, b0, nb, L, G, P, all, keep, kept_tokens, s);
+    const bool all = keep_all != 0, unit = unit_mass != 0, last = keep_last != 0;
+    if (nb <= kSelThreads) select_one<1>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
+    else if (nb <= 2 * kSelThreads) select_one<2>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
+    else if (nb <= 4 * kSelThreads) select_one<4>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
+    else if (nb <= 8 * kSelThreads) select_one<8>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
+    else if (nb <= 16 * kSelThreads) select_one<16>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
+    else select_one<32>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
 }
 
 }  // namespace
 
 cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const int32_t *cu_seqlens,
-                          int num_seqs, int G, double p, uint8_t *keep, int32_t *kept_tokens,
-                          unsigned int *err, cudaStream_t st) {
+                          int num_seqs, int G, bool top_k, double p, int k, bool keep_last,
+                          uint8_t *keep, int32_t *kept_tokens, unsigned int *err, cudaStream_t st) {
     if (num_seqs <= 0) return cudaSuccess;
     static_assert(UP_SELECT_MAX_BLOCKS <= 32 * kSelThreads, "select keeps at most 32 keys per thread");
     static_assert(UP_SELECT_MAX_BLOCKS <= 65536, "the radix search covers 16 index bits");
-    const bool all = !(p < 1.0);
-    // P = ceil(p * 2^62): p * 2^62 is exact in fp64, so this is the exact threshold
-    const unsigned long long P = all ? 0ull : (unsigned long long)ceil(p * 4611686018427387904.0);
+    bool all;
+    unsigned long long P;
+    if (top_k) {
+        all = k >= UP_SELECT_MAX_BLOCKS;  // every sequence that fits keeps everything
+        P = (unsigned long long)k;
+    } else {
+        all = !(p < 1.0);
+        // P = ceil(p * 2^62): p * 2^62 is exact in fp64, so this is the exact threshold
+        P = all ? 0ull : (unsigned long long)ceil(p * 4611686018427387904.0);
+    }
     return launch_pdl(select_topp_kernel, dim3(num_seqs), dim3(kSelThreads), 0, st, scores,
-                      cu_blocks, cu_seqlens, G, P, all ? 1 : 0, keep, kept_tokens, err);
+                      cu_blocks, cu_seqlens, G, P, top_k ? 1 : 0, all ? 1 : 0, keep_last ? 1 : 0,
+                      keep, kept_tokens, err);
 }
 
 }  // namespace up

@@ -131,6 +131,38 @@ up_status up_select_topp(const float *scores, const int32_t *cu_blocks,
                          const int32_t *cu_seqlens, int num_seqs, int G, double p,
                          uint8_t *keep, int32_t *kept_tokens, up_stream_t stream);
 
+/* Selection rule of up_select_blocks. */
+typedef enum { UP_SELECT_TOP_P = 0, UP_SELECT_TOP_K = 1 } up_select_mode;
+
+/* up_select_blocks flag: also keep the last block of every non-empty sequence. */
+#define UP_SELECT_KEEP_LAST 0x1u
+
+/*
+ * Block selection, general form.
+ *
+ * Sources: UniPrefill overview, top-p selection paragraph (top-p),
+ * hyper-parameters paragraph (its ablation sets top-p against keeping a fixed
+ * number of blocks: top-k), system-integration paragraph (decode continues
+ * from the end of each sequence: the keep-last option).
+ *
+ * Blocks are ranked per sequence exactly as in up_select_topp (score
+ * descending, block index ascending).
+ *   mode UP_SELECT_TOP_P  the kept set of up_select_topp with threshold p
+ *                         (0 < p; k is ignored).
+ *   mode UP_SELECT_TOP_K  the first min(k, nb_s) ranks (k >= 1; p is ignored).
+ *   flags                 0, or UP_SELECT_KEEP_LAST: after the rule, the last
+ *                         block of every non-empty sequence is kept too and
+ *                         counted in kept_tokens (the method as the pages state
+ *                         it leaves this off).
+ * The other arguments, outputs and device errors are those of up_select_topp;
+ * an unknown mode or flag bit, p <= 0 or NaN in top-p mode, or k < 1 in top-k
+ * mode return UP_ERR_INVALID_ARG before any launch.
+ */
+up_status up_select_blocks(const float *scores, const int32_t *cu_blocks,
+                           const int32_t *cu_seqlens, int num_seqs, int G, up_select_mode mode,
+                           double p, int k, uint32_t flags, uint8_t *keep, int32_t *kept_tokens,
+                           up_stream_t stream);
+
 /*
  * Compaction (sparsity propagation).
  *

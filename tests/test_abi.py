@@ -90,6 +90,18 @@ def test_select_and_compact_reject_bad_arguments(L):
     assert L.up_select_topp(_fake(), _fake(), _fake(), 1, 40, 0.9, _fake(), _fake(), None) == 2
     assert L.up_select_topp(None, _fake(), _fake(), 1, 64, 0.9, _fake(), _fake(), None) == 1
 
+    def sel(mode=0, p=0.9, k=4, flags=0, G=64, sc=_fake()):
+        return L.up_select_blocks(sc, _fake(), _fake(), 1, G, mode, p, k, flags, _fake(), _fake(),
+                                  None)
+
+    assert sel(mode=2) == 1              # unknown mode
+    assert sel(flags=0x2) == 1           # unknown flag bit
+    assert sel(mode=0, p=0.0) == 1
+    assert sel(mode=0, p=float("nan")) == 1
+    assert sel(mode=1, k=0) == 1
+    assert sel(mode=1, G=40) == 2
+    assert sel(mode=1, sc=None) == 1
+
     def comp(hidden=512, x=_fake(), xo=_fake(), ws=_fake(), wsb=1 << 30, G=64, tk=_fake()):
         return L.up_compact(x, _fake(), hidden, _fake(), 1, 4096, G, _fake(), _fake(), xo,
                             _fake(), _fake(), None, tk, ws, wsb, None)

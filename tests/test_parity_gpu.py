@@ -100,6 +100,18 @@ def _golden_topp():
     return out
 
 
+def _golden_topk():
+    out = []
+    with open(os.path.join(os.path.dirname(__file__), "golden", "topk_hand_enumerated.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, sc, kept = (x.strip() for x in line.split(";"))
+                out.append((int(k), [float(v) for v in sc.split(",")],
+                            sorted(int(v) for v in kept.split(","))))
+    return out
+
+
 @pytest.mark.parametrize("p,scores,kept", _golden_topp())
 def test_select_hand_enumerated(p, scores, kept):
     nb, G = len(scores), 16
@@ -240,3 +252,97 @@ def test_ex2_rate_probe():
     (a GB300 runs tens of ex2 per clock per SM on 152 SMs at ~2 GHz)."""
     rate = up.measure_ex2_rate()
     assert 1e11 < rate < 1e15
+
+
+def gpu_select_blocks(scores_np, cb_np, cu_np, G, **kw):
+    sc = torch.from_numpy(np.ascontiguousarray(scores_np, dtype=np.float32)).cuda()
+    keep, kt = up.select_blocks(sc, torch.from_numpy(np.ascontiguousarray(cb_np, np.int32)).cuda(),
+                                torch.from_numpy(np.ascontiguousarray(cu_np, np.int32)).cuda(), G, **kw)
+    torch.cuda.synchronize()
+    return keep[: len(scores_np)].cpu().numpy(), kt[: len(cu_np) - 1].cpu().numpy()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("k,scores,kept", _golden_topk())
+def test_select_topk_hand_enumerated(k, scores, kept):
+    nb, G = len(scores), 16
+    keep, kt = gpu_select_blocks(np.array(scores), np.array([0, nb]), np.array([0, nb * G]), G,
+                                 mode="top_k", k=k)
+    assert sorted(np.nonzero(keep)[0].tolist()) == kept
+    assert kt.tolist() == [len(kept) * G]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("nb", [1, 2, 513, 1024, 1025, 4096, 16384])
+def test_select_topk_ties_and_sizes(nb):
+    """Top-k on scores with many exact ties, at every power-of-two size boundary of
+    the kernel, against the oracle on the same fp32 scores (unique result)."""
+    rng = np.random.default_rng(nb + 7)
+    vals = np.array([1.0, 0.5, 0.25, 0.125], dtype=np.float32)
+    sc = vals[rng.integers(0, 4, size=nb)].astype(np.float64)
+    sc = (sc / sc.sum()).astype(np.float32).astype(np.float64)
+    G = 64
+    cu = np.array([0, nb * G - 5], np.int32)
+    cb = np.array([0, nb], np.int32)
+    for k in sorted({1, 2, max(1, nb // 3), nb - 1 if nb > 1 else 1, nb, nb + 5}):
+        keep, kt = gpu_select_blocks(sc, cb, cu, G, mode="top_k", k=k)
+        ok, okt = oracle.select_topk(sc, cb, cu, G, k)
+        np.testing.assert_array_equal(keep, ok)
+        assert kt.tolist() == okt.tolist()
+
+
+@pytest.mark.gpu
+def test_select_topk_varlen_random_scores():
+    """Varlen batch (including an empty sequence) of continuous random scores."""
+    rng = np.random.default_rng(11)
+    lens = [640, 0, 4100, 64, 131072]
+    G = 64
+    cu = np.array([0] + list(np.cumsum(lens)), np.int32)
+    nbs = [(L + G - 1) // G for L in lens]
+    cb = np.array([0] + list(np.cumsum(nbs)), np.int32)
+    parts = []
+    for nb in nbs:
+        r = rng.exponential(size=nb) ** 2
+        parts.append(r / r.sum() if nb else r)
+    sc = np.concatenate(parts).astype(np.float32).astype(np.float64)
+    for k in (1, 5, 41, 3000):
+        keep, kt = gpu_select_blocks(sc, cb, cu, G, mode="top_k", k=k)
+        ok, okt = oracle.select_topk(sc, cb, cu, G, k)
+        np.testing.assert_array_equal(keep, ok)
+        assert kt.tolist() == okt.tolist()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("mode", ["top_p", "top_k"])
+def test_select_keep_last_option(mode):
+    """The keep-last flag equals the oracle's selection followed by its keep-last
+    step, for both rules, on a varlen batch with ragged last blocks."""
+    rng = np.random.default_rng(5)
+    lens = [1000, 37, 0, 5000, 64]
+    G = 64
+    cu = np.array([0] + list(np.cumsum(lens)), np.int32)
+    nbs = [(L + G - 1) // G for L in lens]
+    cb = np.array([0] + list(np.cumsum(nbs)), np.int32)
+    parts = []
+    for nb in nbs:
+        r = rng.exponential(size=nb) ** 3
+        parts.append(r / r.sum() if nb else r)
+    sc = np.concatenate(parts).astype(np.float32).astype(np.float64)
+    if mode == "top_p":
+        keep, kt = gpu_select_blocks(sc, cb, cu, G, mode="top_p", p=0.9, keep_last=True)
+        ok, okt, ci, ce = oracle.select_topp(sc, cb, cu, G, 0.9)
+        hard, _ = keep_mismatch(keep, oracle.keep_last_block(ok, okt, cb, cu, G)[0], ci, ce, 0.9)
+        assert hard == 0
+        ok2, okt2 = oracle.keep_last_block(ok, okt, cb, cu, G)
+        if np.array_equal(keep, ok2):
+            assert kt.tolist() == okt2.tolist()
+    else:
+        keep, kt = gpu_select_blocks(sc, cb, cu, G, mode="top_k", k=3, keep_last=True)
+        ok, okt = oracle.select_topk(sc, cb, cu, G, 3)
+        ok2, okt2 = oracle.keep_last_block(ok, okt, cb, cu, G)
+        np.testing.assert_array_equal(keep, ok2)
+        assert kt.tolist() == okt2.tolist()
+    # every non-empty sequence keeps its last block
+    for s in range(len(lens)):
+        if nbs[s]:
+            assert keep[cb[s + 1] - 1] == 1
