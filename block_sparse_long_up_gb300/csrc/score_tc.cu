@@ -140,6 +140,9 @@ __device__ void role_tma_k(const CUtensorMap *tmap, const ScoreParams &p, Shared
                            uint8_t *kbuf, int units) {
     using C = Cfg<D>;
     volatile int *abort = &sh.abort;
+    // K is read exactly once: its lines should leave L2 before the block
+    // partials, which the finalize reads back
+    const uint64_t policy = l2_policy_evict_first();
     uint32_t it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         Unit un;
@@ -151,8 +154,8 @@ __device__ void role_tma_k(const CUtensorMap *tmap, const ScoreParams &p, Shared
                 const uint32_t ph = (it / C::kStages) & 1;
                 if (!mbar_wait(smem_u32(&sh.kempty[st]), ph ^ 1, abort, kWaitLimit)) goto done;
                 mbar_arrive_expect_tx(smem_u32(&sh.kfull[st]), kPanelBytesK);
-                tma_load_2d(smem_u32(kbuf + st * kPanelBytesK), tmap, un.j * D + pn * 64, row0,
-                            smem_u32(&sh.kfull[st]));
+                tma_load_2d_hint(smem_u32(kbuf + st * kPanelBytesK), tmap, un.j * D + pn * 64,
+                                 row0, smem_u32(&sh.kfull[st]), policy);
             }
         }
     }
@@ -313,17 +316,20 @@ __device__ __forceinline__ void mask_group(float (&v)[32], int key, int a) {
     for (int i = 0; i < 32; ++i) v[i] = (key + i > a) ? -INFINITY : v[i];
 }
 
-// One predicated store (no branch, so the group code stays one basic block).
-__device__ __forceinline__ void st_if(float *p, float v, bool ok) {
+// One predicated store (no branch, so the group code stays one basic block),
+// with an L2 evict-last policy: the finalize reads the partials back.
+__device__ __forceinline__ void st_if(float *p, float v, bool ok, uint64_t policy) {
     asm volatile(
-        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.global.f32 [%0], %1;\n\t}" ::"l"(p),
-        "f"(v), "r"((int)ok)
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+        "@q st.global.L2::cache_hint.f32 [%0], %1, %3;\n\t}" ::"l"(p),
+        "f"(v), "r"((int)ok), "l"(policy)
         : "memory");
 }
 
 // Per-row state of one row tile within a unit.
 struct RowState {
     float *part;  // partial sums of this row: part[b * R]
+    uint64_t policy;  // L2 policy of the partial stores
     float ref, lsum, acc;
     uint64_t bias2;
     int a;        // causal limit (absolute key position)
@@ -371,15 +377,15 @@ __device__ __forceinline__ void softmax_tile(const Unit &un, RowState &rs, uint3
         exp_sums(cur, s2, rs.bias2, lo, hi);
         if constexpr (G == 16) {
             const int b = kb / 16;
-            st_if(rs.part + (int64_t)b * sq.R, lo, rs.valid && b < sq.nb);
-            st_if(rs.part + (int64_t)(b + 1) * sq.R, hi, rs.valid && b + 1 < sq.nb);
+            st_if(rs.part + (int64_t)b * sq.R, lo, rs.valid && b < sq.nb, rs.policy);
+            st_if(rs.part + (int64_t)(b + 1) * sq.R, hi, rs.valid && b + 1 < sq.nb, rs.policy);
             rs.lsum += lo;
             rs.lsum += hi;
         } else {
             rs.acc += lo + hi;
             if ((t * kGroups + cg + 1) % kGroupsPerBlock == 0) {
                 const int b = (kb + 32 - G) / G;
-                st_if(rs.part + (int64_t)b * sq.R, rs.acc, rs.valid && b < sq.nb);
+                st_if(rs.part + (int64_t)b * sq.R, rs.acc, rs.valid && b < sq.nb, rs.policy);
                 rs.lsum += rs.acc;
                 rs.acc = 0.f;
             }
@@ -417,8 +423,8 @@ __device__ __forceinline__ void softmax_tile_fast(RowState &rs, uint32_t taddr, 
         float lo, hi;
         exp_sums(cur, s2, rs.bias2, lo, hi);
         if constexpr (G == 16) {
-            st_if(pb + (int64_t)(2 * cg) * R, lo, rs.valid);
-            st_if(pb + (int64_t)(2 * cg + 1) * R, hi, rs.valid);
+            st_if(pb + (int64_t)(2 * cg) * R, lo, rs.valid, rs.policy);
+            st_if(pb + (int64_t)(2 * cg + 1) * R, hi, rs.valid, rs.policy);
             rs.lsum += lo;
             rs.lsum += hi;
         } else {
@@ -428,7 +434,7 @@ __device__ __forceinline__ void softmax_tile_fast(RowState &rs, uint32_t taddr, 
             if (closes) {
                 // the closing block's index relative to the step's first block
                 const int off = G <= 128 ? ((cg + 1) * 32 / G - 1) : 0;
-                st_if(pb + (int64_t)off * R, rs.acc, rs.valid);
+                st_if(pb + (int64_t)off * R, rs.acc, rs.valid, rs.policy);
                 rs.lsum += rs.acc;
                 rs.acc = 0.f;
             }
@@ -458,6 +464,7 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
     const bool row_used = row < p.g * p.tpt;
     const float s = p.scale_log2;
     const uint64_t s2 = pack2(s, s);
+    const uint64_t part_policy = l2_policy_evict_last();
     uint32_t gstep = 0, tpar = 0u;  // bit b: parity of the uses of TMEM buffer b so far
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         Unit un;
@@ -473,6 +480,7 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
             rs[pr].a = sq.L - sq.ns + (rs[pr].valid ? tq : 0);
             rs[pr].r = (int64_t)un.j * grows + (int64_t)tq * p.g + h;
             rs[pr].part = p.part + sq.part_off + rs[pr].r;
+            rs[pr].policy = part_policy;
             rs[pr].ref = -INFINITY;
             rs[pr].lsum = 0.f;
             rs[pr].acc = 0.f;
