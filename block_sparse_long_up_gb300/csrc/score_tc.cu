@@ -240,6 +240,19 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
             it += C::kPanels;
             const bool mine = C::kPairs == 2 ? pair_ok : ((gstep & 1u) == (uint32_t)w);
             if (C::kPairs == 1 && !mine) continue;  // the other issuer's step and stages
+            // Every K panel of the step (and the Q tiles) are in shared memory
+            // before the first MMA, and the stage releases come after the last:
+            // the issue queue is shallow, so a barrier check or a commit between
+            // two MMAs of the buffer fill leaves the tensor pipe idle.  These
+            // checks come before the wait for the TMEM buffer, while the softmax
+            // warpgroups still hold it (the ring runs steps ahead, so they
+            // almost never block); the fill starts as soon as the buffer is free.
+            for (int pn = 0; pn < C::kPanels; ++pn) {
+                const uint32_t i = it0 + pn;
+                if (!mbar_wait(smem_u32(&sh.kfull[i % C::kStages]), (i / C::kStages) & 1, abort,
+                               kWaitLimit))
+                    goto out;
+            }
             if (mine) {
                 if (!q_ready) {
                     if (!mbar_wait(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort, kWaitLimit))
@@ -249,14 +262,9 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
                 if (!mbar_wait(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, kWaitLimit))
                     goto out;
                 tc_fence_after();
-            }
-            for (int pn = 0; pn < C::kPanels; ++pn) {
-                const uint32_t i = it0 + pn;
-                const int st = i % C::kStages;
-                if (!mbar_wait(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort, kWaitLimit))
-                    goto out;
-                if (mine) {
-                    tc_fence_after();
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn) {
+                    const int st = (it0 + pn) % C::kStages;
                     const uint64_t bd = smem_desc_sw128(smem_u32(kbuf + st * kPanelBytesK));
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -268,12 +276,11 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
                                      idesc, (pn | ks) != 0);
                     }
                 }
-                mma_commit(smem_u32(&sh.kempty[st]));
-            }
-            if (mine) {
                 mma_commit(smem_u32(&sh.tfull[w]));
-                ++tuse;
             }
+            for (int pn = 0; pn < C::kPanels; ++pn)
+                mma_commit(smem_u32(&sh.kempty[(it0 + pn) % C::kStages]));
+            if (mine) ++tuse;
         }
         // the pair buffer is free once this issuer's MMAs on it have completed
         if (C::kPairs == 1 || pair_ok) mma_commit(smem_u32(&sh.qempty[qs]));
@@ -406,9 +413,15 @@ __device__ __forceinline__ void softmax_tile(const Unit &un, RowState &rs, uint3
 // branch inside, so the compiler can overlap one group's sums with the next
 // group's exponentials.  skey is a multiple of 128 and of G when G <= 128; a
 // 256-key block closes at the end of every second step of the unit.
+// It also tests, without waiting, whether the next slot's TMEM buffer is ready
+// (barrier next_bar, phase parity next_par) before its last group's arithmetic,
+// so the barrier's latency overlaps that work; the caller skips its own wait
+// when next_ready comes back true.
 template <int G>
 __device__ __forceinline__ void softmax_tile_fast(RowState &rs, uint32_t taddr, int skey, int t,
-                                                  int R, uint64_t s2, Shared &sh, int buf) {
+                                                  int R, uint64_t s2, Shared &sh, int buf,
+                                                  uint32_t next_bar, uint32_t next_par,
+                                                  bool &next_ready) {
     constexpr int kGroups = kStepKeys / 32;
     constexpr int kGroupsPerBlock = G >= 32 ? G / 32 : 1;
     float *const pb = rs.part + (int64_t)(skey / G) * R;  // the step's first block
@@ -420,6 +433,7 @@ __device__ __forceinline__ void softmax_tile_fast(RowState &rs, uint32_t taddr, 
         float(&cur)[32] = (cg & 1) ? vb : va;
         float(&nxt)[32] = (cg & 1) ? va : vb;
         if (cg + 1 < kGroups) tmem_ld32(taddr + (cg + 1) * 32, nxt);
+        if (cg + 1 == kGroups) next_ready = mbar_test_wait(next_bar, next_par);
         float lo, hi;
         exp_sums(cur, s2, rs.bias2, lo, hi);
         if constexpr (G == 16) {
@@ -466,6 +480,7 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
     const uint64_t s2 = pack2(s, s);
     const uint64_t part_policy = l2_policy_evict_last();
     uint32_t gstep = 0, tpar = 0u;  // bit b: parity of the uses of TMEM buffer b so far
+    bool next_ready = false;        // the next slot's buffer was seen ready in advance
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         Unit un;
         decode_unit<D>(p, u, un);
@@ -491,8 +506,9 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
             for (int pr = 0; pr < C::kPairs; ++pr) {
                 if (pr >= un.npairs) break;
                 const int buf = C::kPairs == 2 ? pr : (int)(gstep & 1u);
-                const bool ok =
-                    mbar_wait(smem_u32(&sh.tfull[buf]), (tpar >> buf) & 1u, abort, kWaitLimit);
+                const bool ok = next_ready || mbar_wait(smem_u32(&sh.tfull[buf]),
+                                                        (tpar >> buf) & 1u, abort, kWaitLimit);
+                next_ready = false;
                 __syncwarp();  // tcgen05.ld is warp-collective: reconverge after polling
                 if (!__all_sync(0xffffffffu, ok)) return;
                 tpar ^= 1u << buf;
@@ -502,8 +518,15 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
                 const int skey = un.k0 + t * kStepKeys;
                 if (t == 0 || skey + kStepKeys - 1 > sq.L - sq.ns)
                     softmax_tile<G>(un, rs[pr], taddr, t, s2, s, sh, buf);
-                else
-                    softmax_tile_fast<G>(rs[pr], taddr, skey, t, sq.R, s2, sh, buf);
+                else {
+                    // the next slot: the unit's next pair, else pair 0 of the next
+                    // step or unit (head_dim <= 128); the next step's buffer (256)
+                    const int nbuf = C::kPairs == 2 ? (pr + 1 < un.npairs ? pr + 1 : 0)
+                                                    : (int)((gstep + 1) & 1u);
+                    softmax_tile_fast<G>(rs[pr], taddr, skey, t, sq.R, s2, sh, buf,
+                                         smem_u32(&sh.tfull[nbuf]), (tpar >> nbuf) & 1u,
+                                         next_ready);
+                }
             }
         }
 #pragma unroll
