@@ -20,9 +20,9 @@
 // mass-before is < P (top-p: P = ceil(p * 2^62)).  K* is found by a radix search over the
 // key's digits, most significant first.  Each pass histograms the exact masses
 // (and counts) of the keys that share the digits found so far over the next
-// 8-bit digit (lanes of a warp holding the same digit combine their masses
-// first, so the shared-memory atomics stay few even when the leading digits
-// barely vary); the last non-empty bucket whose mass-before is < P holds K*
+// 8-bit digit (a warp first adds the masses of its lanes that share a digit,
+// so the shared-memory atomics stay few even when the leading digits barely
+// vary); the last non-empty bucket whose mass-before is < P holds K*
 // (the first key of that bucket is kept; the first key of any later bucket is
 // not).  A bucket holding a single key ends the search.  Six passes at most:
 // four over the 32 score bits, two over the block index (< 2^16).
@@ -52,16 +52,28 @@ __device__ __forceinline__ unsigned long long key_fixed(unsigned long long key) 
     return sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0ull);
 }
 
+// Shared state of one selection.  Bucket masses are kept as four 16-bit
+// pieces (each sum < 2^30 for <= 2^14 keys) plus counts.
+struct SelectShared {
+    alignas(16) unsigned int hpart[4][256];
+    alignas(16) unsigned int hcnt[256];
+    unsigned long long s_prefix, s_base, s_kstar;
+    unsigned int s_cnt;
+    int shi[32];
+};
+
 template <int E>
 __device__ void select_one(const float *__restrict__ scores, int b0, int nb, int L, int G,
                            unsigned long long P, bool unit_mass, bool keep_all, bool keep_last,
-                           uint8_t *__restrict__ keep, int32_t *kept_tokens, int s) {
-    // bucket masses as four 16-bit pieces (each < 2^30 for <= 2^14 keys) and counts
-    __shared__ unsigned int hpart[4][256];
-    __shared__ unsigned int hcnt[256];
-    __shared__ unsigned long long s_prefix, s_base, s_kstar;
-    __shared__ unsigned int s_cnt;
-    __shared__ int shi[32];
+                           uint8_t *__restrict__ keep, int32_t *kept_tokens, int s,
+                           SelectShared &sh) {
+    auto &hpart = sh.hpart;
+    auto &hcnt = sh.hcnt;
+    auto &s_prefix = sh.s_prefix;
+    auto &s_base = sh.s_base;
+    auto &s_kstar = sh.s_kstar;
+    auto &s_cnt = sh.s_cnt;
+    auto &shi = sh.shi;
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     // the rank key's high word per key; its low word is the index t + i * kSelThreads
     unsigned khi[E];
@@ -90,34 +102,66 @@ __device__ void select_one(const float *__restrict__ scores, int b0, int nb, int
             for (int i = 0; i < E; ++i) {
                 const int e = t + i * kSelThreads;
                 const bool match = ps == 0 || (key(i) >> (sh + 8)) == (prefix >> (sh + 8));
-                // 256 = not in the searched range; lanes with equal digits add
-                // their masses together and one of them updates the bucket
+                // 256 = not in the searched range.  A warp aggregates by digit:
+                // in up to four rounds it takes the digit of its lowest pending
+                // lane, adds the masses of all lanes holding that digit with a
+                // shuffle tree, and one lane updates the bucket; lanes still
+                // pending after that update their own buckets.  The leading
+                // digits take few distinct values per warp, so few atomics hit
+                // the shared histogram.
                 const unsigned dgt = (e < nb && match) ? (unsigned)((key(i) >> sh) & 255u) : 256u;
-                const unsigned peers = __match_any_sync(0xffffffffu, dgt);
                 const unsigned long long fx =
                     dgt < 256u ? (unit_mass ? 1ull : key_fixed(key(i))) : 0ull;
-                unsigned piece[4];
+                unsigned pending = __ballot_sync(0xffffffffu, dgt < 256u);
+#pragma unroll 1
+                for (int round = 0; round < 4 && pending; ++round) {
+                    const int leader = __ffs(pending) - 1;
+                    const unsigned d = __shfl_sync(0xffffffffu, dgt, leader);
+                    const bool mine = dgt == d;
+                    const unsigned peers = __ballot_sync(0xffffffffu, mine);
+                    unsigned long long v = mine ? fx : 0ull;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    piece[k] = __reduce_add_sync(peers, (unsigned)(fx >> (16 * k)) & 0xFFFFu);
-                if (dgt < 256u && lane == __ffs(peers) - 1) {
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == leader) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) atomicAdd(&hpart[k][dgt], piece[k]);
-                    atomicAdd(&hcnt[dgt], (unsigned)__popc(peers));
+                        for (int k = 0; k < 4; ++k)
+                            atomicAdd(&hpart[k][d], (unsigned)(v >> (16 * k)) & 0xFFFFu);
+                        atomicAdd(&hcnt[d], (unsigned)__popc(peers));
+                    }
+                    pending &= ~peers;
+                }
+                if ((pending >> lane) & 1u) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        atomicAdd(&hpart[k][dgt], (unsigned)(fx >> (16 * k)) & 0xFFFFu);
+                    atomicAdd(&hcnt[dgt], 1u);
                 }
             }
             __syncthreads();
             if (wid == 0) {
-                // lane l owns buckets 8l .. 8l+7: exclusive scan of the lane totals
-                auto bucket_mass = [&](int bkt) {
-                    return (unsigned long long)hpart[0][bkt] +
-                           ((unsigned long long)hpart[1][bkt] << 16) +
-                           ((unsigned long long)hpart[2][bkt] << 32) +
-                           ((unsigned long long)hpart[3][bkt] << 48);
+                // lane l owns buckets 8l .. 8l+7 (read as 16-byte vectors):
+                // exclusive scan of the lane totals
+                unsigned pc[4][8], cc[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 a = reinterpret_cast<const uint4 *>(&hpart[k][8 * lane])[0];
+                    const uint4 b = reinterpret_cast<const uint4 *>(&hpart[k][8 * lane])[1];
+                    pc[k][0] = a.x; pc[k][1] = a.y; pc[k][2] = a.z; pc[k][3] = a.w;
+                    pc[k][4] = b.x; pc[k][5] = b.y; pc[k][6] = b.z; pc[k][7] = b.w;
+                }
+                {
+                    const uint4 a = reinterpret_cast<const uint4 *>(&hcnt[8 * lane])[0];
+                    const uint4 b = reinterpret_cast<const uint4 *>(&hcnt[8 * lane])[1];
+                    cc[0] = a.x; cc[1] = a.y; cc[2] = a.z; cc[3] = a.w;
+                    cc[4] = b.x; cc[5] = b.y; cc[6] = b.z; cc[7] = b.w;
+                }
+                auto bucket_mass = [&](int j) {
+                    return (unsigned long long)pc[0][j] + ((unsigned long long)pc[1][j] << 16) +
+                           ((unsigned long long)pc[2][j] << 32) + ((unsigned long long)pc[3][j] << 48);
                 };
                 unsigned long long tot = 0ull;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) tot += bucket_mass(8 * lane + j);
+                for (int j = 0; j < 8; ++j) tot += bucket_mass(j);
                 unsigned long long x = tot;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -130,15 +174,16 @@ __device__ void select_one(const float *__restrict__ scores, int b0, int nb, int
                 unsigned best_c = 0u;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const unsigned cj = hcnt[8 * lane + j];
-                    if (cj > 0u && S < P) {
+                    if (cc[j] > 0u && S < P) {
                         best = 8 * lane + j;
                         best_S = S;
-                        best_c = cj;
+                        best_c = cc[j];
                     }
-                    S += bucket_mass(8 * lane + j);
+                    S += bucket_mass(j);
                 }
-                const int top = (int)__reduce_max_sync(0xffffffffu, (unsigned)(best + 1)) - 1;
+                int top = best;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) top = max(top, __shfl_xor_sync(0xffffffffu, top, o));
                 if (best == top && best >= 0) {
                     s_prefix = prefix | ((unsigned long long)best << sh);
                     s_base = best_S;
@@ -206,12 +251,13 @@ select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__
         return;
     }
     const bool all = keep_all != 0, unit = unit_mass != 0, last = keep_last != 0;
-    if (nb <= kSelThreads) select_one<1>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
-    else if (nb <= 2 * kSelThreads) select_one<2>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
-    else if (nb <= 4 * kSelThreads) select_one<4>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
-    else if (nb <= 8 * kSelThreads) select_one<8>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
-    else if (nb <= 16 * kSelThreads) select_one<16>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
-    else select_one<32>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s);
+    __shared__ SelectShared sh;
+    if (nb <= kSelThreads) select_one<1>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    else if (nb <= 2 * kSelThreads) select_one<2>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    else if (nb <= 4 * kSelThreads) select_one<4>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    else if (nb <= 8 * kSelThreads) select_one<8>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    else if (nb <= 16 * kSelThreads) select_one<16>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    else select_one<32>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
 }
 
 }  // namespace
