@@ -25,7 +25,8 @@
 // vary); the last non-empty bucket whose mass-before is < P holds K*
 // (the first key of that bucket is kept; the first key of any later bucket is
 // not).  A bucket holding a single key ends the search.  Six passes at most:
-// four over the 32 score bits, two over the block index (< 2^16).
+// four over the 31 score bits (the first is the exponent), two over the block
+// index (< 2^16).
 #include "../../include/up.h"
 #include "common.cuh"
 
@@ -36,14 +37,16 @@ namespace {
 constexpr int kSelThreads = 512;
 
 __device__ __forceinline__ unsigned long long rank_key(float score, int idx) {
-    // scores are >= 0; -0, NaN and anything not > 0 rank as 0
+    // scores are >= 0; -0, NaN and anything not > 0 rank as 0.  The score bits
+    // of a non-negative float fit in 31 bits, so the key's top bit is always 0
+    // and its first radix digit (bits 55..62) is exactly the float's exponent.
     const unsigned bits = score > 0.f ? __float_as_uint(score) : 0u;
-    return ((unsigned long long)(0xFFFFFFFFu - bits) << 32) | (unsigned)idx;
+    return ((unsigned long long)(0x7FFFFFFFu - bits) << 32) | (unsigned)idx;
 }
 
 // score * 2^62 truncated, from the key's score bits; scores >= 1 count as 1.
 __device__ __forceinline__ unsigned long long key_fixed(unsigned long long key) {
-    const unsigned bits = 0xFFFFFFFFu - (unsigned)(key >> 32);
+    const unsigned bits = 0x7FFFFFFFu - (unsigned)(key >> 32);
     if (bits >= 0x3F800000u) return 1ull << 62;
     const int e = (int)(bits >> 23);
     if (e == 0) return 0ull;  // zero or subnormal (< 2^-126)
@@ -91,7 +94,9 @@ __device__ void select_one(const float *__restrict__ scores, int b0, int nb, int
         bool single = false;
 #pragma unroll 1
         for (int ps = 0; ps < 6; ++ps) {
-            const int sh = ps < 4 ? 56 - 8 * ps : 40 - 8 * ps;  // 56, 48, 40, 32, 8, 0
+            // digits: exponent (55..62), mantissa 47..54, 39..46, 32..39 (bit 39 is
+            // already fixed by then), then the block index (16 bits)
+            const int sh = ps < 3 ? 55 - 8 * ps : (ps == 3 ? 32 : 40 - 8 * ps);  // 55,47,39,32,8,0
             if (t < 256) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) hpart[k][t] = 0u;
