@@ -227,7 +227,7 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     if (up::launch_score_main(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     if (t_kernel_stop && cudaEventRecord(t_kernel_stop, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_fallback(p, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
-    if (up::launch_score_finalize(p, lay, s) != cudaSuccess) return UP_ERR_CUDA;
+    if (up::launch_score_finalize(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     return UP_OK;
 }
 

@@ -135,7 +135,8 @@ cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, con
 cudaError_t launch_score_main(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
                               cudaStream_t st);
 cudaError_t launch_score_fallback(const ScoreParams &p, int num_sms, cudaStream_t st);
-cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, cudaStream_t st);
+cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
+                                  cudaStream_t st);
 // top_k: keep the first k ranks (p unused); otherwise top-p with p.
 cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const int32_t *cu_seqlens,
                           int num_seqs, int G, bool top_k, double p, int k, bool keep_last,

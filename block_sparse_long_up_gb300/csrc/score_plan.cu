@@ -203,29 +203,21 @@ finalize_rows_kernel(ScoreParams p) {
 }
 
 // Block scores.  score_b = sum_r part[b][r] * w[c(b)][r], with c(b) the chunk
-// of block b.  A CTA takes two blocks; four warps share a block, warp q taking
-// the q-th quarter of its rows as float4 groups (eight loads of part and eight
-// of w in flight per lane) into 4 interleaved accumulators, combined in a fixed
-// order, then a fixed butterfly, then the four quarters in order: bitwise
-// reproducible.
-constexpr int kBlocksPerCta = 2;
-constexpr int kWarpsPerBlock = 4;
+// of block b.  A CTA takes a contiguous run of the blocks and walks it in
+// batches of up to kFinBatch blocks of one sequence and one chunk: a batch
+// shares one weight row, read once (the next batch of the same chunk finds it
+// in L1), and all of its partials are in flight together.  Thread t takes the
+// float4 groups t, t + 256, t + 512, ... of the rows, in increasing order, into
+// one accumulator per block; a fixed butterfly and the eight warps in order
+// finish the sum.  The order depends neither on the grid nor on the batching,
+// so the result is bitwise reproducible.
+constexpr int kFinThreads = 256;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kFinBatch = 4;      // blocks per batch
+constexpr int kFinUnroll = 4;     // float4 groups per thread and block in flight
+constexpr int kFinCtasPerSm = 4;
 
-// Ties 8 float4 values to this point of the program: every use of them comes
-// after it, so the loads that produce them are all issued before any use.
-__device__ __forceinline__ void hold8(float4 (&v)[8]) {
-    asm volatile(""
-                 : "+f"(v[0].x), "+f"(v[0].y), "+f"(v[0].z), "+f"(v[0].w), "+f"(v[1].x),
-                   "+f"(v[1].y), "+f"(v[1].z), "+f"(v[1].w), "+f"(v[2].x), "+f"(v[2].y),
-                   "+f"(v[2].z), "+f"(v[2].w), "+f"(v[3].x), "+f"(v[3].y), "+f"(v[3].z),
-                   "+f"(v[3].w), "+f"(v[4].x), "+f"(v[4].y), "+f"(v[4].z), "+f"(v[4].w),
-                   "+f"(v[5].x), "+f"(v[5].y), "+f"(v[5].z), "+f"(v[5].w), "+f"(v[6].x),
-                   "+f"(v[6].y), "+f"(v[6].z), "+f"(v[6].w), "+f"(v[7].x), "+f"(v[7].y),
-                   "+f"(v[7].z), "+f"(v[7].w));
-}
-
-// 16-byte loads issued in program order (so a batch is in flight together):
-// streaming (partials, read once) and read-only cached (weights).
+// 16-byte loads: streaming (partials, read once) and read-only cached (weights).
 __device__ __forceinline__ float4 ld_stream4(const float4 *p) {
     float4 v;
     asm volatile("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -241,6 +233,13 @@ __device__ __forceinline__ float4 ld_ro4(const float4 *p) {
     return v;
 }
 
+__device__ __forceinline__ float dot4(const float4 x, const float4 y, float a) {
+    a = fmaf(x.x, y.x, a);
+    a = fmaf(x.y, y.y, a);
+    a = fmaf(x.z, y.z, a);
+    return fmaf(x.w, y.w, a);
+}
+
 __device__ __forceinline__ int find_seq_by_block(const SeqInfo *seqs, int B, int gb) {
     int lo = 0, hi = B - 1;
     while (lo < hi) {
@@ -250,77 +249,83 @@ __device__ __forceinline__ int find_seq_by_block(const SeqInfo *seqs, int B, int
     return lo;
 }
 
-__global__ void __launch_bounds__(kBlocksPerCta * kWarpsPerBlock * 32)
-finalize_blocks_kernel(ScoreParams p) {
-    __shared__ float red[kBlocksPerCta][kWarpsPerBlock];
+__global__ void __launch_bounds__(kFinThreads) finalize_blocks_kernel(ScoreParams p) {
+    __shared__ float red[2][kFinBatch][kFinWarps];
     pdl_trigger();
     pdl_wait();
     const int nbt = p.counters->blocks;  // 0 when the plan is invalid
+    const int per = (nbt + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int lo = (int)blockIdx.x * per, hi = min(lo + per, nbt);
+    if (lo >= hi) return;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int lb = wid / kWarpsPerBlock, q = wid % kWarpsPerBlock;
-    for (int g0 = blockIdx.x * kBlocksPerCta; g0 < nbt; g0 += gridDim.x * kBlocksPerCta) {
-        const int gb = g0 + lb;
-        float t = 0.f;
-        if (gb < nbt) {
-            const SeqInfo sq = p.seqs[find_seq_by_block(p.seqs, p.num_seqs, gb)];
-            const int b = gb - sq.blk_off;
-            const float *wr = p.mref + sq.stat_off + (int64_t)block_slot(b, p.G, p.C) * sq.R;
-            const float *pt = p.part + sq.part_off + (int64_t)b * sq.R;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if ((sq.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(wr) & 15) == 0) &&
-                ((reinterpret_cast<uintptr_t>(pt) & 15) == 0)) {
-                const float4 *pt4 = reinterpret_cast<const float4 *>(pt);
-                const float4 *w4 = reinterpret_cast<const float4 *>(wr);
-                const int R4 = sq.R / 4;
-                const int per = (R4 + kWarpsPerBlock - 1) / kWarpsPerBlock;
-                const int lo = q * per, hi = min(lo + per, R4);
-                int i = lo + lane;
-                for (; i + 7 * 32 < hi; i += 8 * 32) {  // full batches: 16 loads in flight
-                    float4 x[8], y[8];
+    const int bpc = p.C / p.G;  // blocks per key chunk
+    int s = find_seq_by_block(p.seqs, p.num_seqs, lo);
+    SeqInfo sq = p.seqs[s];
+    int par = 0;
+    for (int gb = lo; gb < hi; par ^= 1) {
+        while (gb >= sq.blk_off + sq.nb) sq = p.seqs[++s];  // skips empty sequences
+        const int b = gb - sq.blk_off;
+        const int nbat = min(min(kFinBatch, hi - gb), min(sq.nb - b, (b / bpc + 1) * bpc - b));
+        const float *wr = p.mref + sq.stat_off + (int64_t)block_slot(b, p.G, p.C) * sq.R;
+        const float *pt = p.part + sq.part_off + (int64_t)b * sq.R;
+        float acc[kFinBatch];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        x[k] = ld_stream4(pt4 + i + k * 32);
-                        y[k] = ld_ro4(w4 + i + k * 32);
+        for (int k = 0; k < kFinBatch; ++k) acc[k] = 0.f;
+        if ((sq.R % 4 == 0) && ((reinterpret_cast<uintptr_t>(wr) & 15) == 0) &&
+            ((reinterpret_cast<uintptr_t>(pt) & 15) == 0)) {
+            const float4 *w4 = reinterpret_cast<const float4 *>(wr);
+            const float4 *p4 = reinterpret_cast<const float4 *>(pt);
+            const int R4 = sq.R / 4;
+            const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i0 = threadIdx.x; i0 < R4; i0 += kFinUnroll * kFinThreads) {
+                float4 w[kFinUnroll], x[kFinBatch][kFinUnroll];
+#pragma unroll
+                for (int u = 0; u < kFinUnroll; ++u) {
+                    const int i = i0 + u * kFinThreads;
+                    w[u] = i < R4 ? ld_ro4(w4 + i) : zero;
+                }
+#pragma unroll
+                for (int k = 0; k < kFinBatch; ++k)
+#pragma unroll
+                    for (int u = 0; u < kFinUnroll; ++u) {
+                        const int i = i0 + u * kFinThreads;
+                        x[k][u] = (k < nbat && i < R4) ? ld_stream4(p4 + (int64_t)k * R4 + i)
+                                                       : zero;
                     }
-                    hold8(x);
-                    hold8(y);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float &a = acc[k & 3];
-                        a = fmaf(x[k].x, y[k].x, a);
-                        a = fmaf(x[k].y, y[k].y, a);
-                        a = fmaf(x[k].z, y[k].z, a);
-                        a = fmaf(x[k].w, y[k].w, a);
-                    }
-                }
-                for (; i < hi; i += 32) {  // tail
-                    const float4 x = __ldcs(pt4 + i), y = __ldg(w4 + i);
-                    acc[0] = fmaf(x.x, y.x, acc[0]);
-                    acc[0] = fmaf(x.y, y.y, acc[0]);
-                    acc[0] = fmaf(x.z, y.z, acc[0]);
-                    acc[0] = fmaf(x.w, y.w, acc[0]);
-                }
-            } else {
-                const int per = (sq.R + kWarpsPerBlock - 1) / kWarpsPerBlock;
-                const int lo = q * per, hi = min(lo + per, sq.R);
-                for (int r = lo + lane; r < hi; r += 4 * 32) {
+                for (int k = 0; k < kFinBatch; ++k)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (r + k * 32 < hi)
-                            acc[k] = fmaf(__ldcs(pt + r + k * 32), __ldg(wr + r + k * 32), acc[k]);
-                }
+                    for (int u = 0; u < kFinUnroll; ++u) acc[k] = dot4(x[k][u], w[u], acc[k]);
             }
-            t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        } else {
+            for (int r = threadIdx.x; r < sq.R; r += kFinThreads) {
+                const float w = __ldg(wr + r);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                for (int k = 0; k < kFinBatch; ++k)
+                    if (k < nbat) acc[k] = fmaf(__ldcs(pt + (int64_t)k * sq.R + r), w, acc[k]);
+            }
         }
-        if (lane == 0) red[lb][q] = t;
-        __syncthreads();
-        if (threadIdx.x < kBlocksPerCta && g0 + (int)threadIdx.x < nbt) {
-            const float *rq = red[threadIdx.x];
-            p.scores[g0 + threadIdx.x] = (rq[0] + rq[1]) + (rq[2] + rq[3]);
+#pragma unroll
+        for (int k = 0; k < kFinBatch; ++k) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
         }
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < kFinBatch; ++k) red[par][k][wid] = acc[k];
+        }
+        // one barrier per batch: red is double-buffered, and a buffer is written
+        // again only after the next batch's barrier, which its readers reach
+        // after reading it
         __syncthreads();
+        if ((int)threadIdx.x < nbat) {
+            const float *rq = red[par][threadIdx.x];
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < kFinWarps; ++w) t += rq[w];
+            p.scores[gb + threadIdx.x] = t;
+        }
+        gb += nbat;
     }
 }
 
@@ -333,7 +338,8 @@ cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, con
                       p.num_seqs, total_tokens, p.Hq, p.Hk, p.d, p.n, p.G, p.C, p.err);
 }
 
-cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, cudaStream_t st) {
+cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
+                                  cudaStream_t st) {
     if (lay.max_rows > 0) {
         const int64_t want = (lay.max_rows + kRowsPerCta - 1) / kRowsPerCta;
         const int grid = (int)(want < 65535 ? want : 65535);
@@ -342,11 +348,10 @@ cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, 
         if (e != cudaSuccess) return e;
     }
     if (lay.max_blocks > 0) {
-        // two blocks per CTA (CTAs past the real block count exit at once)
-        const int64_t want = (lay.max_blocks + kBlocksPerCta - 1) / kBlocksPerCta;
-        const int grid = (int)(want < 65535 ? want : 65535);
-        return launch_pdl(finalize_blocks_kernel, dim3(grid),
-                          dim3(kBlocksPerCta * kWarpsPerBlock * 32), 0, st, p);
+        // a contiguous run of blocks per CTA (CTAs past the real block count exit at once)
+        const int64_t cap = (int64_t)kFinCtasPerSm * num_sms;
+        const int grid = (int)(lay.max_blocks < cap ? lay.max_blocks : cap);
+        return launch_pdl(finalize_blocks_kernel, dim3(grid), dim3(kFinThreads), 0, st, p);
     }
     return cudaSuccess;
 }
