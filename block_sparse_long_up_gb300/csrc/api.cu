@@ -93,8 +93,6 @@ up::ScoreLayout score_layout(int B, int64_t total, int Hq, int Hk, int d, int n,
     L.part = off;     off = align256(off + sizeof(float) * (size_t)L.max_part);
     L.mref = off;     off = align256(off + sizeof(float) * (size_t)L.max_stat);
     L.lsum = off;     off = align256(off + sizeof(float) * (size_t)L.max_stat);
-    L.rowm = off;     off = align256(off + sizeof(float) * (size_t)(L.max_rows > 0 ? L.max_rows : 1));
-    L.rowinv = off;   off = align256(off + sizeof(float) * (size_t)(L.max_rows > 0 ? L.max_rows : 1));
     L.flags = off;    off = align256(off + sizeof(int32_t) * (size_t)(32 * L.max_units + 16));
     L.total = off;
     return L;
@@ -209,8 +207,6 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     p.part = reinterpret_cast<float *>(ws + lay.part);
     p.mref = reinterpret_cast<float *>(ws + lay.mref);
     p.lsum = reinterpret_cast<float *>(ws + lay.lsum);
-    p.rowm = reinterpret_cast<float *>(ws + lay.rowm);
-    p.rowinv = reinterpret_cast<float *>(ws + lay.rowinv);
     p.scores = scores;
     p.flag_list = reinterpret_cast<int32_t *>(ws + lay.flags);
     p.max_units = (int)lay.max_units;
@@ -226,7 +222,7 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     if (t_kernel_start && cudaEventRecord(t_kernel_start, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_main(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     if (t_kernel_stop && cudaEventRecord(t_kernel_stop, s) != cudaSuccess) return UP_ERR_CUDA;
-    if (up::launch_score_fallback(p, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
+    if (up::launch_score_finish(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_finalize(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     return UP_OK;
 }
@@ -242,7 +238,7 @@ up_status up_select_topp(const float *scores, const int32_t *cu_blocks,
     up_status st = device_state(&ds);
     if (st != UP_OK) return st;
     if (up::launch_select(scores, cu_blocks, cu_seqlens, num_seqs, G, false, p, 0, false, keep,
-                          kept_tokens, ds->err, reinterpret_cast<cudaStream_t>(stream)) !=
+                          kept_tokens, ds->err, ds->sms, reinterpret_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return UP_ERR_CUDA;
     return UP_OK;
@@ -267,7 +263,7 @@ up_status up_select_blocks(const float *scores, const int32_t *cu_blocks,
     up_status st = device_state(&ds);
     if (st != UP_OK) return st;
     if (up::launch_select(scores, cu_blocks, cu_seqlens, num_seqs, G, mode == UP_SELECT_TOP_K, p,
-                          k, (flags & UP_SELECT_KEEP_LAST) != 0, keep, kept_tokens, ds->err,
+                          k, (flags & UP_SELECT_KEEP_LAST) != 0, keep, kept_tokens, ds->err, ds->sms,
                           reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return UP_ERR_CUDA;
     return UP_OK;

@@ -9,14 +9,17 @@
 
 namespace up {
 
-// Programmatic dependent launch.  Every kernel of the library calls
-// pdl_trigger() first, so the next kernel of the stream may be scheduled while
-// this one still runs, and pdl_wait() before its first global-memory access:
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// the attribute and calls pdl_wait() before its first global-memory access:
 // that waits until the previous kernel of the stream has finished and its
 // writes are visible (read-after-write and write-after-read alike).  Work before
 // pdl_wait() touches only on-chip state (shared memory, barriers, TMEM) and
-// kernel parameters.  Both are no-ops for a kernel launched without the
-// attribute.
+// kernel parameters.  A kernel that calls pdl_trigger() lets the next kernel's
+// CTAs be scheduled (up to their own pdl_wait()) while it still runs; one that
+// does not releases them as its CTAs exit.  Only the one-warp plan kernel
+// triggers early, so the scoring kernel's prologue overlaps it: everywhere else
+// early-scheduled CTAs that only wait measured slower than a release at exit.
+// Both calls are no-ops for a kernel launched without the attribute.
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -64,7 +67,8 @@ struct Counters {
     int32_t blocks;      // sum nb_s
     int64_t rows;        // sum R_s
     int32_t flagged;     // units queued for the exact fallback
-    int32_t pad[11];
+    int32_t fin_done;    // CTAs of the finishing kernel done with the fallback (flagged case)
+    int32_t pad[10];
 };
 static_assert(sizeof(Counters) == 64, "Counters is 64 bytes");
 
@@ -93,7 +97,7 @@ __host__ __device__ __forceinline__ int block_slot(int b, int G, int C) {
 
 // Score workspace layout (offsets in bytes, every region 256-byte aligned).
 struct ScoreLayout {
-    size_t seqs, counters, part, mref, lsum, rowm, rowinv, flags, total;
+    size_t seqs, counters, part, mref, lsum, flags, total;
     int64_t max_part, max_stat, max_rows, max_units, max_blocks, total_tokens;
     int64_t max_qrows;  // upper bound on the rows of q_last (sum of n_s)
     int chunk;  // C: keys per work unit
@@ -108,8 +112,6 @@ struct ScoreParams {
     float *part;   // [b][r] per sequence: block partial sums (relative to mref)
     float *mref;   // [c][r] per sequence: reference (log2 units) of the chunk's partials
     float *lsum;   // [c][r] per sequence: sum of the chunk's partials
-    float *rowm;   // [global row]: the row's softmax maximum (log2 units)
-    float *rowinv; // [global row]: 1 / (row softmax sum * n_s * Hq)
     float *scores;
     int32_t *flag_list;  // 4*unit + row tile of tiles whose sums overflowed (exact fallback)
     int max_units;
@@ -134,13 +136,16 @@ cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, con
                               int64_t total_tokens, cudaStream_t st);
 cudaError_t launch_score_main(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
                               cudaStream_t st);
-cudaError_t launch_score_fallback(const ScoreParams &p, int num_sms, cudaStream_t st);
+// the exact fallback for queued tiles, then the row statistics and chunk weights
+cudaError_t launch_score_finish(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
+                               cudaStream_t st);
 cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
                                   cudaStream_t st);
 // top_k: keep the first k ranks (p unused); otherwise top-p with p.
 cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const int32_t *cu_seqlens,
                           int num_seqs, int G, bool top_k, double p, int k, bool keep_last,
-                          uint8_t *keep, int32_t *kept_tokens, unsigned int *err, cudaStream_t st);
+                          uint8_t *keep, int32_t *kept_tokens, unsigned int *err, int num_sms,
+                          cudaStream_t st);
 
 struct CompactArgs {
     const uint4 *x;

@@ -47,7 +47,6 @@ __device__ int64_t block_excl_scan_i64(int64_t v, int64_t *total, int64_t *sh) {
 // starting destination row and list slot, and it writes its range.
 __global__ void __launch_bounds__(kIndexThreads)
 compact_index_kernel(CompactArgs a) {
-    pdl_trigger();
     pdl_wait();
     __shared__ int64_t sh[32];
     const int B = a.num_seqs;
@@ -100,7 +99,6 @@ compact_index_kernel(CompactArgs a) {
 
 __global__ void __launch_bounds__(kGatherThreads)
 compact_gather_kernel(CompactArgs a) {
-    pdl_trigger();
     pdl_wait();
     const int K = *a.nkept;
     const int64_t items = (int64_t)K * a.items_per_block;

@@ -1,13 +1,24 @@
-// score_simt.cu -- exact CUDA-core fallback for score work units.
+// score_fallback.cu -- the kernel that finishes the scoring statistics after
+// the tensor-core kernel: an exact CUDA-core fallback for the rare overflowed
+// tiles, then each softmax row's normaliser and the weights of its chunks.
 //
-// The tensor-core kernel measures every partial sum against a reference taken
-// from the first 32 keys of a work unit.  If a later key of the same unit has a
-// logit more than ~115 binary orders of magnitude above that reference, its fp32
-// sums overflow; the kernel then queues that 128-row tile here.  This kernel
-// recomputes such a tile with two passes over the logits: the first finds each
-// row's exact maximum m over the unit's keys (log2 units), the second sums
-// 2^(z*log2e/sqrt(d) - m) over every block.  The queue is empty for ordinary
-// attention logits.
+// Fallback.  The tensor-core kernel measures every partial sum against a
+// reference taken from the first 32 keys of a work unit.  If a later key of the
+// same unit has a logit more than ~115 binary orders of magnitude above that
+// reference, its fp32 sums overflow; the kernel then queues that 128-row tile
+// here.  The tile is recomputed with two passes over the logits: the first
+// finds each row's exact maximum m over the unit's keys (log2 units), the
+// second sums 2^(z*log2e/sqrt(d) - m) over every block.  The queue is empty for
+// ordinary attention logits.
+//
+// Rows.  Per row r of a sequence, over its key chunks c:
+//     m_r = max_c mref[c][r],  l_r = sum_c lsum[c][r] * 2^(mref[c][r] - m_r),
+//     inv_r = 1 / (l_r * n_s * Hq)   (the softmax normaliser and the query/head mean)
+// and then, in place of mref[c][r], the weight of chunk c's partial sums:
+//     w[c][r] = 2^(mref[c][r] - m_r) * inv_r.
+// With an empty queue every CTA goes straight to the rows; otherwise the CTA
+// that finishes its queued tiles last (a counter the plan kernel zeroes) does
+// all rows after every recomputed tile is in memory.
 // Source: UniPrefill overview, block-wise importance estimation paragraph.
 #include "common.cuh"
 
@@ -29,12 +40,120 @@ __device__ __forceinline__ void tile_logits(const __nv_bfloat16 *qT, const float
     }
 }
 
+// Rows: a pass takes 64 consecutive rows, lane l holding rows l and l + 32;
+// the four warps take every fourth chunk slot and merge (max, sum) online, then
+// warp 0 merges the four partial results in warp order -- a fixed order, so the
+// result is bitwise reproducible.  The first kCached chunk maxima of each
+// (row, warp) stay in registers for the weight pass.
+constexpr int kRowsPerPass = 64;
+constexpr int kSlotLanes = kRowsPerTile / 32;
+constexpr int kCached = 8;
+
+__device__ __forceinline__ void merge_ms(float &m, float &l, float mc, float lc) {
+    if (mc == -INFINITY) return;
+    if (m == -INFINITY) { m = mc; l = lc; return; }
+    const float mn = fmaxf(m, mc);
+    l = l * exp2f(m - mn) + lc * exp2f(mc - mn);
+    m = mn;
+}
+
+__device__ __forceinline__ int find_seq_by_row(const SeqInfo *seqs, int B, int64_t r) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (seqs[mid].row_off <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ float chunk_weight(float mc, float M, float inv) {
+    return (mc == -INFINITY || inv == 0.f) ? 0.f : exp2f(mc - M) * inv;
+}
+
+// Every pass of CTAs cta, cta + ncta, ... over the `total` rows.  Loads go
+// through L2 (.cg): in the queued case they read what other CTAs of this
+// kernel wrote.
+__device__ __forceinline__ void finalize_rows(const ScoreParams &p, int64_t total, int cta,
+                                              int ncta) {
+    __shared__ float sm[kSlotLanes][kRowsPerPass], sl[kSlotLanes][kRowsPerPass];
+    __shared__ float sM[kRowsPerPass], sI[kRowsPerPass];
+    __shared__ int sR[kRowsPerPass];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int64_t g0 = (int64_t)cta * kRowsPerPass; g0 < total;
+         g0 += (int64_t)ncta * kRowsPerPass) {
+        int nsl[2], R[2];
+        float *mr[2];
+        const float *ls[2];
+        float m[2], l[2], mc[2][kCached];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t gr = g0 + lane + 32 * h;
+            const bool ok = gr < total;
+            const SeqInfo &sq = p.seqs[find_seq_by_row(p.seqs, p.num_seqs, ok ? gr : total - 1)];
+            const int64_t r = (ok ? gr : total - 1) - sq.row_off;
+            nsl[h] = ok ? sq.nchunks * kSlotsPerChunk : 0;
+            R[h] = sq.R;
+            mr[h] = p.mref + sq.stat_off + r;
+            ls[h] = p.lsum + sq.stat_off + r;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+            float lc[kCached];
+#pragma unroll
+            for (int i = 0; i < kCached; ++i) {
+                const int c = wid + kSlotLanes * i;
+                mc[h][i] = c < nsl[h] ? __ldcg(mr[h] + (int64_t)c * R[h]) : -INFINITY;
+                lc[i] = c < nsl[h] ? __ldcg(ls[h] + (int64_t)c * R[h]) : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < kCached; ++i) merge_ms(m[h], l[h], mc[h][i], lc[i]);
+            for (int c = wid + kSlotLanes * kCached; c < nsl[h]; c += kSlotLanes)
+                merge_ms(m[h], l[h], __ldcg(mr[h] + (int64_t)c * R[h]),
+                         __ldcg(ls[h] + (int64_t)c * R[h]));
+            sm[wid][lane + 32 * h] = m[h];
+            sl[wid][lane + 32 * h] = l[h];
+            if (wid == 0) sR[lane + 32 * h] = R[h];
+        }
+        __syncthreads();
+        if (wid < 2) {
+            const int i = lane + 32 * wid;
+            float M = sm[0][i], Lsum = sl[0][i];
+#pragma unroll
+            for (int w = 1; w < kSlotLanes; ++w) merge_ms(M, Lsum, sm[w][i], sl[w][i]);
+            sM[i] = M;
+            // rows past the total have no chunks: M = -inf, inv 0, nothing written
+            sI[i] = (M == -INFINITY || !(Lsum > 0.f)) ? 0.f : 1.0f / (Lsum * (float)sR[i]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float M = sM[lane + 32 * h], inv = sI[lane + 32 * h];
+#pragma unroll
+            for (int i = 0; i < kCached; ++i) {
+                const int c = wid + kSlotLanes * i;
+                if (c < nsl[h]) mr[h][(int64_t)c * R[h]] = chunk_weight(mc[h][i], M, inv);
+            }
+            for (int c = wid + kSlotLanes * kCached; c < nsl[h]; c += kSlotLanes) {
+                float *q = mr[h] + (int64_t)c * R[h];
+                *q = chunk_weight(__ldcg(q), M, inv);
+            }
+        }
+        __syncthreads();
+    }
+}
+
 template <int D>
-__global__ void __launch_bounds__(kRowsPerTile)
-score_fallback_kernel(ScoreParams p) {
-    pdl_trigger();
+__global__ void __launch_bounds__(kRowsPerTile, 4)
+score_finish_kernel(ScoreParams p) {
     pdl_wait();
     const int nflag = min(p.counters->flagged, p.flag_cap);
+    const int64_t total_rows = p.counters->rows;
+    if (nflag == 0) {
+        finalize_rows(p, total_rows, blockIdx.x, gridDim.x);
+        return;
+    }
     extern __shared__ __align__(16) unsigned char smem[];
     __nv_bfloat16 *qT = reinterpret_cast<__nv_bfloat16 *>(smem);                 // [D][128]
     float *ks = reinterpret_cast<float *>(smem + D * kRowsPerTile * 2);          // [32][D]
@@ -111,24 +230,39 @@ score_fallback_kernel(ScoreParams p) {
             p.lsum[o] = lsum;
         }
     }
+    // every CTA's recomputed tiles are in memory before the last one reads them
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&const_cast<Counters *>(p.counters)->fin_done, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        finalize_rows(p, total_rows, 0, 1);
+    }
 }
 
 template <int D>
-cudaError_t launch_d(const ScoreParams &p, int num_sms, cudaStream_t st) {
+cudaError_t launch_d(const ScoreParams &p, int64_t max_rows, int num_sms, cudaStream_t st) {
     const size_t smem = (size_t)D * kRowsPerTile * 2 + (size_t)kKeyTile * D * 4;
-    cudaError_t e = cudaFuncSetAttribute(score_fallback_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(score_finish_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(score_fallback_kernel<D>, dim3(num_sms), dim3(kRowsPerTile), smem, st, p);
+    // one 64-row pass per CTA for the rows, at least one CTA per SM for the queue
+    const int64_t passes = (max_rows + kRowsPerPass - 1) / kRowsPerPass;
+    const int64_t want = passes > num_sms ? passes : num_sms;
+    const int grid = (int)(want < 65535 ? want : 65535);
+    return launch_pdl(score_finish_kernel<D>, dim3(grid), dim3(kRowsPerTile), smem, st, p);
 }
 
 }  // namespace
 
-cudaError_t launch_score_fallback(const ScoreParams &p, int num_sms, cudaStream_t st) {
+cudaError_t launch_score_finish(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
+                               cudaStream_t st) {
     switch (p.d) {
-        case 64: return launch_d<64>(p, num_sms, st);
-        case 128: return launch_d<128>(p, num_sms, st);
-        case 256: return launch_d<256>(p, num_sms, st);
+        case 64: return launch_d<64>(p, lay.max_rows, num_sms, st);
+        case 128: return launch_d<128>(p, lay.max_rows, num_sms, st);
+        case 256: return launch_d<256>(p, lay.max_rows, num_sms, st);
         default: return cudaErrorInvalidValue;
     }
 }

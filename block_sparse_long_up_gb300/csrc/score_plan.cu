@@ -58,7 +58,7 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
         // leave a well-formed empty plan: every later kernel sees no work
         if (lane == 0) {
             atomicOr(err, 0x1u);
-            cnt->units = 0; cnt->blocks = 0; cnt->rows = 0; cnt->flagged = 0;
+            cnt->units = 0; cnt->blocks = 0; cnt->rows = 0; cnt->flagged = 0; cnt->fin_done = 0;
         }
         for (int s = lane; s <= B; s += 32) {
             cu_blocks[s] = 0;
@@ -113,92 +113,7 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
         cnt->blocks = (int32_t)base_b;
         cnt->rows = base_r;
         cnt->flagged = 0;
-    }
-}
-
-__device__ __forceinline__ int find_seq_by_row(const SeqInfo *seqs, int B, int64_t r) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (seqs[mid].row_off <= r) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
-
-// Row statistics and chunk weights.  Per row r of a sequence:
-//     m_r = max_c mref[c][r],  l_r = sum_c lsum[c][r] * 2^(mref[c][r] - m_r),
-//     inv_r = 1 / (l_r * n_s * Hq)   (the softmax normaliser and the query/head mean)
-// and then, in place of mref[c][r], the weight of chunk c's partial sums:
-//     w[c][r] = 2^(mref[c][r] - m_r) * inv_r.
-// A CTA takes 32 consecutive rows; its 8 warps take every 8th chunk slot and
-// merge (max, sum) online, then warp 0 merges the 8 partial results in warp
-// order -- a fixed order, so the result is bitwise reproducible.  rowm/rowinv
-// keep m_r and inv_r.
-constexpr int kRowsPerCta = 32;
-constexpr int kSlotLanes = 8;
-
-__device__ __forceinline__ void merge_ms(float &m, float &l, float mc, float lc) {
-    if (mc == -INFINITY) return;
-    if (m == -INFINITY) { m = mc; l = lc; return; }
-    const float mn = fmaxf(m, mc);
-    l = l * exp2f(m - mn) + lc * exp2f(mc - mn);
-    m = mn;
-}
-
-__global__ void __launch_bounds__(kRowsPerCta * kSlotLanes)
-finalize_rows_kernel(ScoreParams p) {
-    __shared__ float sm[kSlotLanes][kRowsPerCta], sl[kSlotLanes][kRowsPerCta];
-    __shared__ float sM[kRowsPerCta], sI[kRowsPerCta];
-    pdl_trigger();
-    pdl_wait();
-    const int64_t total = p.counters->rows;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int64_t g0 = (int64_t)blockIdx.x * kRowsPerCta; g0 < total;
-         g0 += (int64_t)gridDim.x * kRowsPerCta) {
-        const int64_t gr = g0 + lane;
-        const bool ok = gr < total;
-        float m = -INFINITY, l = 0.f;
-        int nslots = 0, R = 0;
-        float *mr = nullptr;
-        const float *ls = nullptr;
-        if (ok) {
-            const int s = find_seq_by_row(p.seqs, p.num_seqs, gr);
-            const SeqInfo sq = p.seqs[s];
-            const int64_t r = gr - sq.row_off;
-            nslots = sq.nchunks * kSlotsPerChunk;
-            R = sq.R;
-            mr = p.mref + sq.stat_off + r;
-            ls = p.lsum + sq.stat_off + r;
-#pragma unroll 4
-            for (int c = wid; c < nslots; c += kSlotLanes)
-                merge_ms(m, l, mr[(int64_t)c * R], ls[(int64_t)c * R]);
-        }
-        sm[wid][lane] = m;
-        sl[wid][lane] = l;
-        __syncthreads();
-        if (wid == 0) {
-            float M = sm[0][lane], Lsum = sl[0][lane];
-#pragma unroll
-            for (int w = 1; w < kSlotLanes; ++w) merge_ms(M, Lsum, sm[w][lane], sl[w][lane]);
-            const float inv = (M == -INFINITY || !(Lsum > 0.f)) ? 0.f : 1.0f / (Lsum * (float)R);
-            sM[lane] = M;
-            sI[lane] = inv;
-            if (ok) {
-                p.rowm[gr] = M;
-                p.rowinv[gr] = inv;
-            }
-        }
-        __syncthreads();
-        if (ok) {
-            const float M = sM[lane], inv = sI[lane];
-#pragma unroll 4
-            for (int c = wid; c < nslots; c += kSlotLanes) {
-                float *q = mr + (int64_t)c * R;
-                const float mc = *q;
-                *q = (mc == -INFINITY || inv == 0.f) ? 0.f : exp2f(mc - M) * inv;
-            }
-        }
-        __syncthreads();
+        cnt->fin_done = 0;
     }
 }
 
@@ -251,7 +166,6 @@ __device__ __forceinline__ int find_seq_by_block(const SeqInfo *seqs, int B, int
 
 __global__ void __launch_bounds__(kFinThreads) finalize_blocks_kernel(ScoreParams p) {
     __shared__ float red[2][kFinBatch][kFinWarps];
-    pdl_trigger();
     pdl_wait();
     const int nbt = p.counters->blocks;  // 0 when the plan is invalid
     const int per = (nbt + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -340,20 +254,11 @@ cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, con
 
 cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
                                   cudaStream_t st) {
-    if (lay.max_rows > 0) {
-        const int64_t want = (lay.max_rows + kRowsPerCta - 1) / kRowsPerCta;
-        const int grid = (int)(want < 65535 ? want : 65535);
-        cudaError_t e = launch_pdl(finalize_rows_kernel, dim3(grid), dim3(kRowsPerCta * kSlotLanes),
-                                   0, st, p);
-        if (e != cudaSuccess) return e;
-    }
-    if (lay.max_blocks > 0) {
-        // a contiguous run of blocks per CTA (CTAs past the real block count exit at once)
-        const int64_t cap = (int64_t)kFinCtasPerSm * num_sms;
-        const int grid = (int)(lay.max_blocks < cap ? lay.max_blocks : cap);
-        return launch_pdl(finalize_blocks_kernel, dim3(grid), dim3(kFinThreads), 0, st, p);
-    }
-    return cudaSuccess;
+    if (lay.max_blocks <= 0) return cudaSuccess;
+    // a contiguous run of blocks per CTA (CTAs past the real block count exit at once)
+    const int64_t cap = (int64_t)kFinCtasPerSm * num_sms;
+    const int grid = (int)(lay.max_blocks < cap ? lay.max_blocks : cap);
+    return launch_pdl(finalize_blocks_kernel, dim3(grid), dim3(kFinThreads), 0, st, p);
 }
 
 }  // namespace up

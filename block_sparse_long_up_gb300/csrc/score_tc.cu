@@ -570,7 +570,6 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     uint8_t *qbuf = smem;                          // Q buffers (1024-aligned panels)
     uint8_t *kbuf = smem + C::kQBufs * C::kQBytes; // kStages x K panel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {

@@ -27,6 +27,16 @@
 // not).  A bucket holding a single key ends the search.  Six passes at most:
 // four over the 31 score bits (the first is the exponent), two over the block
 // index (< 2^16).
+//
+// Sequences of at most kCmpMaxBlocks blocks skip the search: many CTAs share
+// the sequence, each loads all of its keys into shared memory, and one warp
+// per block takes the exact mass-before of the block directly, as the sum of
+// the masses of every key ranked before it (nb^2 key comparisons, spread over
+// the GPU).  The same rule decides: kept iff mass-before < P.  The block at the
+// last kept rank (mass-before < P and, with its own mass, >= P, or no key ranked
+// after it) writes the sequence's kept tokens, so no CTA waits for another.
+#include <algorithm>
+
 #include "../../include/up.h"
 #include "common.cuh"
 
@@ -35,6 +45,8 @@ namespace up {
 namespace {
 
 constexpr int kSelThreads = 512;
+constexpr int kCmpMaxBlocks = 4096;  // larger sequences take the radix search
+constexpr int kCmpSmem = 2 * kCmpMaxBlocks * (int)sizeof(unsigned long long);
 
 __device__ __forceinline__ unsigned long long rank_key(float score, int idx) {
     // scores are >= 0; -0, NaN and anything not > 0 rank as 0.  The score bits
@@ -233,35 +245,87 @@ __device__ void select_one(const float *__restrict__ scores, int b0, int nb, int
     }
 }
 
-__global__ void __launch_bounds__(kSelThreads)
+// Blocks [x * per, (x + 1) * per) of the sequence, per = ceil(nb / X).
+__device__ void select_compare(const float *__restrict__ scores, int b0, int nb, int L, int G,
+                               unsigned long long P, bool unit_mass, bool keep_all,
+                               bool keep_last, uint8_t *__restrict__ keep,
+                               int32_t *kept_tokens, int s, int x, int X,
+                               unsigned long long *smem) {
+    const int per = (nb + X - 1) / X;
+    const int lo = x * per, hi = min(lo + per, nb);
+    if (lo >= hi) return;
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    if (keep_all) {
+        for (int e = lo + t; e < hi; e += kSelThreads) keep[b0 + e] = 1;
+        if (x == 0 && t == 0) kept_tokens[s] = L;
+        return;
+    }
+    unsigned long long *skey = smem, *sfx = smem + kCmpMaxBlocks;
+#pragma unroll 4
+    for (int e = t; e < nb; e += kSelThreads) {
+        const unsigned long long k = rank_key(scores[b0 + e], e);
+        skey[e] = k;
+        sfx[e] = unit_mass ? 1ull : key_fixed(k);
+    }
+    __syncthreads();
+    for (int i = lo + wid; i < hi; i += kSelThreads / 32) {
+        const unsigned long long ki = skey[i];
+        unsigned long long before = 0ull;
+        bool after = false;  // some key ranks after block i
+#pragma unroll 4
+        for (int j = lane; j < nb; j += 32) {
+            const unsigned long long kj = skey[j];
+            if (kj < ki) before += sfx[j];
+            after |= kj > ki;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+        after = __any_sync(0xffffffffu, after);
+        const bool in = before < P;
+        if (lane == 0) keep[b0 + i] = (in || (keep_last && i == nb - 1)) ? 1 : 0;
+        if (in && (!after || before + sfx[i] >= P)) {  // the last kept rank
+            int tok = 0;
+            for (int j = lane; j < nb; j += 32)
+                if (skey[j] <= ki || (keep_last && j == nb - 1)) tok += min(G, L - j * G);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) tok += __shfl_xor_sync(0xffffffffu, tok, o);
+            if (lane == 0) kept_tokens[s] = tok;
+        }
+    }
+}
+
+// grid (X, num_seqs): CTA x of sequence blockIdx.y.
+__global__ void __launch_bounds__(kSelThreads, 2)
 select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__ cu_blocks,
                    const int32_t *__restrict__ cu, int G, unsigned long long P, int unit_mass,
                    int keep_all, int keep_last, uint8_t *__restrict__ keep,
                    int32_t *__restrict__ kept_tokens, unsigned int *err) {
-    pdl_trigger();
+    extern __shared__ __align__(16) unsigned long long cmp_smem[];
     pdl_wait();
-    const int s = blockIdx.x;
+    const int s = blockIdx.y, x = blockIdx.x;
     const int b0 = cu_blocks[s];
     const int nb = cu_blocks[s + 1] - b0;
     const int L = cu[s + 1] - cu[s];
     if (nb <= 0) {
-        if (threadIdx.x == 0) kept_tokens[s] = 0;
+        if (x == 0 && threadIdx.x == 0) kept_tokens[s] = 0;
         return;
     }
     if (nb > UP_SELECT_MAX_BLOCKS) {
-        if (threadIdx.x == 0) {
+        if (x == 0 && threadIdx.x == 0) {
             atomicOr(err, UP_DEVERR_SELECT_TOO_MANY_BLOCKS);
             kept_tokens[s] = 0;
         }
         return;
     }
     const bool all = keep_all != 0, unit = unit_mass != 0, last = keep_last != 0;
+    if (nb <= kCmpMaxBlocks) {
+        select_compare(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, x,
+                       (int)gridDim.x, cmp_smem);
+        return;
+    }
+    if (x != 0) return;
     __shared__ SelectShared sh;
-    if (nb <= kSelThreads) select_one<1>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
-    else if (nb <= 2 * kSelThreads) select_one<2>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
-    else if (nb <= 4 * kSelThreads) select_one<4>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
-    else if (nb <= 8 * kSelThreads) select_one<8>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
-    else if (nb <= 16 * kSelThreads) select_one<16>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    if (nb <= 16 * kSelThreads) select_one<16>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
     else select_one<32>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
 }
 
@@ -269,10 +333,12 @@ select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__
 
 cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const int32_t *cu_seqlens,
                           int num_seqs, int G, bool top_k, double p, int k, bool keep_last,
-                          uint8_t *keep, int32_t *kept_tokens, unsigned int *err, cudaStream_t st) {
+                          uint8_t *keep, int32_t *kept_tokens, unsigned int *err, int num_sms,
+                          cudaStream_t st) {
     if (num_seqs <= 0) return cudaSuccess;
     static_assert(UP_SELECT_MAX_BLOCKS <= 32 * kSelThreads, "select keeps at most 32 keys per thread");
     static_assert(UP_SELECT_MAX_BLOCKS <= 65536, "the radix search covers 16 index bits");
+    static_assert(kCmpMaxBlocks == 8 * kSelThreads, "the radix search starts above the compare path");
     bool all;
     unsigned long long P;
     if (top_k) {
@@ -283,9 +349,15 @@ cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const i
         // P = ceil(p * 2^62): p * 2^62 is exact in fp64, so this is the exact threshold
         P = all ? 0ull : (unsigned long long)ceil(p * 4611686018427387904.0);
     }
-    return launch_pdl(select_topp_kernel, dim3(num_seqs), dim3(kSelThreads), 0, st, scores,
-                      cu_blocks, cu_seqlens, G, P, top_k ? 1 : 0, all ? 1 : 0, keep_last ? 1 : 0,
-                      keep, kept_tokens, err);
+    const cudaError_t attr = cudaFuncSetAttribute(
+        select_topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCmpSmem);
+    if (attr != cudaSuccess) return attr;
+    // about two CTAs per SM over all sequences (at most 4096 per sequence)
+    const int X = std::max(1, std::min(4096, (2 * num_sms + num_seqs - 1) / num_seqs));
+    if (num_seqs > 65535) return cudaErrorInvalidValue;
+    return launch_pdl(select_topp_kernel, dim3(X, num_seqs), dim3(kSelThreads), (size_t)kCmpSmem,
+                      st, scores, cu_blocks, cu_seqlens, G, P, top_k ? 1 : 0, all ? 1 : 0,
+                      keep_last ? 1 : 0, keep, kept_tokens, err);
 }
 
 }  // namespace up

@@ -120,7 +120,7 @@ def test_select_hand_enumerated(p, scores, kept):
     assert kt.tolist() == [len(kept) * G]
 
 
-@pytest.mark.parametrize("nb", [1, 2, 1000, 1024, 1025, 4096, 16384])
+@pytest.mark.parametrize("nb", [1, 2, 1000, 1024, 1025, 4096, 4097, 8192, 16384])
 def test_select_ties_and_sizes(nb):
     """Scores with many exact ties (a few distinct values) and all power-of-two
     boundaries of the on-chip sort; the oracle's rule on the same fp32 scores."""
@@ -239,6 +239,10 @@ def test_overflowing_unit_takes_the_exact_fallback():
     torch.cuda.synchronize()
     flagged = int(ws[256 + 16:256 + 20].view(torch.int32).item())
     assert flagged > 0, "the overflowing unit was not queued for the fallback"
+    # with a queue, the CTAs of the finishing kernel count themselves done and
+    # the last one computes the row statistics
+    fin_done = int(ws[256 + 20:256 + 24].view(torch.int32).item())
+    assert fin_done > 0
     orc_sc, orc_cb = oracle.score_blocks(inp.q_last, inp.k, inp.cu_seqlens, 32, 8, 128, 128, 64)
     g_sc = sc[: int(orc_cb[-1])].cpu().numpy().astype(np.float64)
     nbad, worst = score_failures(g_sc, orc_sc)
@@ -273,7 +277,7 @@ def test_select_topk_hand_enumerated(k, scores, kept):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("nb", [1, 2, 513, 1024, 1025, 4096, 16384])
+@pytest.mark.parametrize("nb", [1, 2, 513, 1024, 1025, 4096, 4097, 8192, 16384])
 def test_select_topk_ties_and_sizes(nb):
     """Top-k on scores with many exact ties, at every power-of-two size boundary of
     the kernel, against the oracle on the same fp32 scores (unique result)."""
@@ -289,6 +293,31 @@ def test_select_topk_ties_and_sizes(nb):
         ok, okt = oracle.select_topk(sc, cb, cu, G, k)
         np.testing.assert_array_equal(keep, ok)
         assert kt.tolist() == okt.tolist()
+
+
+@pytest.mark.gpu
+def test_select_topp_varlen_both_paths():
+    """Top-p on a varlen batch whose sequences take both selection paths: up to
+    4096 blocks the per-block exact mass-before over many CTAs, above it the
+    one-CTA radix search (ragged last blocks, an empty sequence)."""
+    rng = np.random.default_rng(23)
+    G = 64
+    lens = [64 * 5000 + 17, 300, 0, 64 * 4096, 64 * 4097 - 3, 64 * 2048]
+    cu = np.array([0] + list(np.cumsum(lens)), np.int32)
+    nbs = [(L + G - 1) // G for L in lens]
+    cb = np.array([0] + list(np.cumsum(nbs)), np.int32)
+    parts = []
+    for nb in nbs:
+        r = rng.exponential(size=nb) ** 3
+        parts.append(r / r.sum() if nb else r)
+    sc = np.concatenate(parts).astype(np.float32).astype(np.float64)
+    for p in (0.5, 0.9, 0.99):
+        keep, kt = gpu_select(sc, cb, cu, G, p)
+        ok, okt, ci, ce = oracle.select_topp(sc, cb, cu, G, p)
+        hard, _ = keep_mismatch(keep, ok, ci, ce, p)
+        assert hard == 0
+        if np.array_equal(keep, ok):
+            assert kt.tolist() == okt.tolist()
 
 
 @pytest.mark.gpu
