@@ -289,9 +289,9 @@ class Sparsifier:
         self.ws_compact = _alloc_ws(compact_workspace(num_seqs, total_tokens, G), dev)
 
     def launches_per_step(self) -> int:
-        # score: plan, tensor-core main, exact fallback, finalize rows, finalize blocks;
+        # score: plan, tensor-core main, finish (exact fallback, row statistics), block sums;
         # select: 1; compact: index, gather
-        return (5 if self.total > 0 and self.num_seqs > 0 else 1) + 1 + 2
+        return (4 if self.total > 0 and self.num_seqs > 0 else 1) + 1 + 2
 
     def run(self, q_last, k, cu_seqlens, x, pos, stream=None):
         score_blocks(q_last, k, cu_seqlens, self.n, self.G, self.scores, self.cu_blocks,
