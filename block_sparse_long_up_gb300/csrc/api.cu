@@ -216,6 +216,20 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     p.tpt = up::tokens_per_tile(p.g);
     p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
     p.err = ds->err;
+    p.cu_seqlens = cu_seqlens;
+    if (num_seqs == 1) {  // the plan's row for the only sequence, from the host's sizes
+        const int64_t L = total_tokens, ns = L < n ? L : n;
+        const int64_t tpt = up::tokens_per_tile(p.g), tpu = up::tiles_per_unit(d);
+        up::SeqInfo &si = p.seq0;
+        si = up::SeqInfo{};
+        si.L = (int32_t)L;
+        si.ns = (int32_t)ns;
+        si.nb = (int32_t)((L + G - 1) / G);
+        si.nchunks = (int32_t)((L + p.C - 1) / p.C);
+        si.mtiles = (int32_t)(((ns + tpt - 1) / tpt + tpu - 1) / tpu);
+        si.R = (int32_t)(Hq * ns);
+        p.units0 = Hk * si.mtiles * si.nchunks;
+    }
     if (up::launch_score_plan(cu_seqlens, cu_blocks, p, total_tokens, s) != cudaSuccess)
         return UP_ERR_CUDA;
     if (num_seqs == 0 || total_tokens == 0) return UP_OK;

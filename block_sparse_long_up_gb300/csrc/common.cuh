@@ -10,16 +10,17 @@
 namespace up {
 
 // Programmatic dependent launch.  Every kernel of the library is launched with
-// the attribute and calls pdl_wait() before its first global-memory access:
-// that waits until the previous kernel of the stream has finished and its
-// writes are visible (read-after-write and write-after-read alike).  Work before
-// pdl_wait() touches only on-chip state (shared memory, barriers, TMEM) and
-// kernel parameters.  A kernel that calls pdl_trigger() lets the next kernel's
-// CTAs be scheduled (up to their own pdl_wait()) while it still runs; one that
-// does not releases them as its CTAs exit.  Only the one-warp plan kernel
-// triggers early, so the scoring kernel's prologue overlaps it: everywhere else
-// early-scheduled CTAs that only wait measured slower than a release at exit.
-// Both calls are no-ops for a kernel launched without the attribute.
+// the attribute and calls pdl_wait() before it reads what the previous kernel
+// of the stream wrote: that waits until that kernel has finished and its
+// writes are visible (read-after-write and write-after-read alike).  A kernel
+// that calls pdl_trigger() lets the next kernel's CTAs be scheduled while it
+// still runs; one that does not releases them as its CTAs exit.  Only the
+// one-warp plan kernel triggers early, right after its own pdl_wait(): every
+// kernel before it is then complete, so the scoring kernel may read the call's
+// inputs (q_last, k, cu_seqlens) and write its own workspace regions before it
+// waits for the plan itself.  Everywhere else early-scheduled CTAs that only
+// wait measured slower than a release at exit.  Both calls are no-ops for a
+// kernel launched without the attribute.
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -109,6 +110,11 @@ struct ScoreParams {
     const __nv_bfloat16 *k;
     const SeqInfo *seqs;
     const Counters *counters;
+    const int32_t *cu_seqlens;
+    // One sequence: its table row and unit count as the plan computes them from
+    // total_tokens (cu_seqlens must then be {0, total_tokens}); unused otherwise.
+    SeqInfo seq0;
+    int units0;
     float *part;   // [b][r] per sequence: block partial sums (relative to mref)
     float *mref;   // [c][r] per sequence: reference (log2 units) of the chunk's partials
     float *lsum;   // [c][r] per sequence: sum of the chunk's partials

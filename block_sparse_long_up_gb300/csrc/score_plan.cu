@@ -42,8 +42,8 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
                   SeqInfo *__restrict__ seqs, Counters *__restrict__ cnt, int B,
                   int64_t total_tokens, int Hq, int Hk, int d, int n, int G, int C,
                   unsigned int *err) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();  // after the wait: every kernel before this one is complete
     const int lane = threadIdx.x;
     const int g = Hq / Hk;
     // validate cu_seqlens

@@ -89,6 +89,7 @@ struct Shared {
     uint64_t tfull[2], tempty[2];
     uint64_t fin[2];
     uint32_t tmem_base;
+    int units;
     int abort;
 };
 
@@ -101,8 +102,11 @@ struct Unit {
 template <int D>
 __device__ __forceinline__ void decode_unit(const ScoreParams &p, int u, Unit &un) {
     using C = Cfg<D>;
-    const int s = find_seq_by_unit(p.seqs, p.num_seqs, u);
-    un.sq = p.seqs[s];
+    if (p.num_seqs == 1) {
+        un.sq = p.seq0;
+    } else {
+        un.sq = p.seqs[find_seq_by_unit(p.seqs, p.num_seqs, u)];
+    }
     int loc = u - un.sq.unit_off;
     un.grp = loc % un.sq.mtiles;  // group of row tiles
     loc /= un.sq.mtiles;
@@ -551,6 +555,7 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
             // this row tile of the unit for the exact fallback
             const bool bad = st.valid && !(st.lsum <= 3.0e38f);
             if (__any_sync(0xffffffffu, bad) && lane == 0) {
+                pdl_wait();  // the plan zeroes the queue counter
                 const int idx = atomicAdd(&const_cast<Counters *>(p.counters)->flagged, 1);
                 if (idx < p.flag_cap) p.flag_list[idx] = 4 * u + 2 * pr + e;
             }
@@ -572,6 +577,16 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        // One sequence: the work is known from the host's sizes once cu_seqlens
+        // is confirmed to be {0, total}, and nothing below needs the plan (the
+        // kernels before it are complete).  Otherwise wait for the plan's table.
+        if (p.num_seqs == 1) {
+            const bool ok = p.cu_seqlens[0] == 0 && p.cu_seqlens[1] == p.seq0.L;
+            sh.units = ok ? p.units0 : 0;
+        } else {
+            pdl_wait();
+            sh.units = p.counters->units;
+        }
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(smem_u32(&sh.kfull[i]), 1);
             mbar_init(smem_u32(&sh.kempty[i]), C::kStageUsers);
@@ -600,8 +615,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
-    pdl_wait();  // the plan (and the kernels before it) are complete from here on
-    const int units = p.counters->units;
+    const int units = sh.units;
+    if (p.num_seqs != 1) pdl_wait();  // every thread past the plan before reading its table
 
     if (warp == kWarpTmaK) {
         if (lane == 0) role_tma_k<D>(&kmap, p, sh, kbuf, units);
@@ -621,6 +636,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         tmem_dealloc(tmem, kTmemCols);
     }
     if (threadIdx.x == 0 && sh.abort) atomicOr(p.err, UP_DEVERR_TIMEOUT);
+    pdl_wait();  // this grid completes after the plan: later kernels read its table
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
