@@ -242,22 +242,14 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
         for (int t = 0; t < un.nsteps; ++t, ++gstep) {
             const uint32_t it0 = it;
             it += C::kPanels;
-            const bool mine = C::kPairs == 2 ? pair_ok : ((gstep & 1u) == (uint32_t)w);
-            if (C::kPairs == 1 && !mine) continue;  // the other issuer's step and stages
-            // Every K panel of the step (and the Q tiles) are in shared memory
-            // before the first MMA, and the stage releases come after the last:
-            // the issue queue is shallow, so a barrier check or a commit between
-            // two MMAs of the buffer fill leaves the tensor pipe idle.  These
-            // checks come before the wait for the TMEM buffer, while the softmax
-            // warpgroups still hold it (the ring runs steps ahead, so they
-            // almost never block); the fill starts as soon as the buffer is free.
-            for (int pn = 0; pn < C::kPanels; ++pn) {
-                const uint32_t i = it0 + pn;
-                if (!mbar_wait(smem_u32(&sh.kfull[i % C::kStages]), (i / C::kStages) & 1, abort,
-                               kWaitLimit))
-                    goto out;
-            }
-            if (mine) {
+            if constexpr (C::kPairs == 1) {
+                // head_dim 256: one pair, steps alternate between the issuers
+                // (buffer = step parity) and a stage is used by its step's
+                // issuer alone.  A step is four K panels and the ring holds six,
+                // so the ring's turnover, not the tensor pipe, sets the pace:
+                // each panel is multiplied as soon as it lands and released right
+                // after its MMAs, so a stage is held ~0.3 us instead of a step.
+                if ((gstep & 1u) != (uint32_t)w) continue;  // the other issuer's step
                 if (!q_ready) {
                     if (!mbar_wait(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort, kWaitLimit))
                         goto out;
@@ -266,9 +258,13 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
                 if (!mbar_wait(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, kWaitLimit))
                     goto out;
                 tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                 for (int pn = 0; pn < C::kPanels; ++pn) {
-                    const int st = (it0 + pn) % C::kStages;
+                    const uint32_t i = it0 + pn;
+                    const int st = i % C::kStages;
+                    if (!mbar_wait(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort, kWaitLimit))
+                        goto out;
+                    tc_fence_after();
                     const uint64_t bd = smem_desc_sw128(smem_u32(kbuf + st * kPanelBytesK));
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -279,12 +275,57 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
                             mma_bf16(d_base + (uint32_t)(e * kStepKeys), ad + 2 * ks, bd + 2 * ks,
                                      idesc, (pn | ks) != 0);
                     }
+                    mma_commit(smem_u32(&sh.kempty[st]));
                 }
                 mma_commit(smem_u32(&sh.tfull[w]));
+                ++tuse;
+            } else {
+                // head_dim <= 128: pair w uses buffer w, and both issuers walk
+                // every K stage.  Every K panel of the step (and the Q tiles) are
+                // in shared memory before the first MMA, and the stage releases
+                // come after the last: the issue queue is shallow, so a barrier
+                // check or a commit between two MMAs of the buffer fill leaves the
+                // tensor pipe idle.  These checks come before the wait for the
+                // TMEM buffer, while the softmax warpgroups still hold it (the ring
+                // runs steps ahead, so they almost never block); the fill starts
+                // as soon as the buffer is free.
+                for (int pn = 0; pn < C::kPanels; ++pn) {
+                    const uint32_t i = it0 + pn;
+                    if (!mbar_wait(smem_u32(&sh.kfull[i % C::kStages]), (i / C::kStages) & 1,
+                                   abort, kWaitLimit))
+                        goto out;
+                }
+                if (pair_ok) {
+                    if (!q_ready) {
+                        if (!mbar_wait(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort,
+                                       kWaitLimit))
+                            goto out;
+                        q_ready = true;
+                    }
+                    if (!mbar_wait(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, kWaitLimit))
+                        goto out;
+                    tc_fence_after();
+#pragma unroll
+                    for (int pn = 0; pn < C::kPanels; ++pn) {
+                        const int st = (it0 + pn) % C::kStages;
+                        const uint64_t bd = smem_desc_sw128(smem_u32(kbuf + st * kPanelBytesK));
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const uint64_t ad = smem_desc_sw128(
+                                smem_u32(qbuf + qs * C::kQPairBytes + e * C::kQTileBytes +
+                                         pn * kPanelBytesQ));
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)  // 4 x K=16 per 64-wide panel (32 B)
+                                mma_bf16(d_base + (uint32_t)(e * kStepKeys), ad + 2 * ks,
+                                         bd + 2 * ks, idesc, (pn | ks) != 0);
+                        }
+                    }
+                    mma_commit(smem_u32(&sh.tfull[w]));
+                }
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    mma_commit(smem_u32(&sh.kempty[(it0 + pn) % C::kStages]));
+                if (pair_ok) ++tuse;
             }
-            for (int pn = 0; pn < C::kPanels; ++pn)
-                mma_commit(smem_u32(&sh.kempty[(it0 + pn) % C::kStages]));
-            if (mine) ++tuse;
         }
         // the pair buffer is free once this issuer's MMAs on it have completed
         if (C::kPairs == 1 || pair_ok) mma_commit(smem_u32(&sh.qempty[qs]));

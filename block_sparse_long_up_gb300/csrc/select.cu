@@ -28,13 +28,15 @@
 // four over the 31 score bits (the first is the exponent), two over the block
 // index (< 2^16).
 //
-// Sequences of at most kCmpMaxBlocks blocks skip the search: many CTAs share
-// the sequence, each loads all of its keys into shared memory, and one warp
-// per block takes the exact mass-before of the block directly, as the sum of
-// the masses of every key ranked before it (nb^2 key comparisons, spread over
-// the GPU).  The same rule decides: kept iff mass-before < P.  The block at the
-// last kept rank (mass-before < P and, with its own mass, >= P, or no key ranked
-// after it) writes the sequence's kept tokens, so no CTA waits for another.
+// A single sequence of at most kCmpMaxBlocks blocks skips the search: about
+// two CTAs per SM share it, each loads all of its keys into shared memory, and
+// one warp per block takes the exact mass-before of the block directly, as the
+// sum of the masses of every key ranked before it (nb^2 key comparisons, spread
+// over the GPU).  The same rule decides: kept iff mass-before < P.  The block at
+// the last kept rank (mass-before < P and, with its own mass, >= P, or no key
+// ranked after it) writes the sequence's kept tokens, so no CTA waits for
+// another.  Several sequences take the search, one CTA each, side by side (an
+// even split of the CTAs over sequences of unequal length measured slower).
 #include <algorithm>
 
 #include "../../include/up.h"
@@ -294,7 +296,7 @@ __device__ void select_compare(const float *__restrict__ scores, int b0, int nb,
     }
 }
 
-// grid (X, num_seqs): CTA x of sequence blockIdx.y.
+// grid (X, num_seqs): CTA x of sequence blockIdx.y (X > 1 only for one sequence).
 __global__ void __launch_bounds__(kSelThreads, 2)
 select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__ cu_blocks,
                    const int32_t *__restrict__ cu, int G, unsigned long long P, int unit_mass,
@@ -318,14 +320,18 @@ select_topp_kernel(const float *__restrict__ scores, const int32_t *__restrict__
         return;
     }
     const bool all = keep_all != 0, unit = unit_mass != 0, last = keep_last != 0;
-    if (nb <= kCmpMaxBlocks) {
+    if (gridDim.x > 1 && nb <= kCmpMaxBlocks) {
         select_compare(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, x,
                        (int)gridDim.x, cmp_smem);
         return;
     }
     if (x != 0) return;
     __shared__ SelectShared sh;
-    if (nb <= 16 * kSelThreads) select_one<16>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    if (nb <= kSelThreads) select_one<1>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    else if (nb <= 2 * kSelThreads) select_one<2>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    else if (nb <= 4 * kSelThreads) select_one<4>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    else if (nb <= 8 * kSelThreads) select_one<8>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
+    else if (nb <= 16 * kSelThreads) select_one<16>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
     else select_one<32>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
 }
 
@@ -338,7 +344,6 @@ cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const i
     if (num_seqs <= 0) return cudaSuccess;
     static_assert(UP_SELECT_MAX_BLOCKS <= 32 * kSelThreads, "select keeps at most 32 keys per thread");
     static_assert(UP_SELECT_MAX_BLOCKS <= 65536, "the radix search covers 16 index bits");
-    static_assert(kCmpMaxBlocks == 8 * kSelThreads, "the radix search starts above the compare path");
     bool all;
     unsigned long long P;
     if (top_k) {
@@ -352,12 +357,12 @@ cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const i
     const cudaError_t attr = cudaFuncSetAttribute(
         select_topp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCmpSmem);
     if (attr != cudaSuccess) return attr;
-    // about two CTAs per SM over all sequences (at most 4096 per sequence)
-    const int X = std::max(1, std::min(4096, (2 * num_sms + num_seqs - 1) / num_seqs));
+    // one sequence: about two CTAs per SM share it; several: one CTA each
+    const int X = num_seqs == 1 ? std::max(2, 2 * num_sms) : 1;
     if (num_seqs > 65535) return cudaErrorInvalidValue;
-    return launch_pdl(select_topp_kernel, dim3(X, num_seqs), dim3(kSelThreads), (size_t)kCmpSmem,
-                      st, scores, cu_blocks, cu_seqlens, G, P, top_k ? 1 : 0, all ? 1 : 0,
-                      keep_last ? 1 : 0, keep, kept_tokens, err);
+    return launch_pdl(select_topp_kernel, dim3(X, num_seqs), dim3(kSelThreads),
+                      X > 1 ? (size_t)kCmpSmem : 0, st, scores, cu_blocks, cu_seqlens, G, P,
+                      top_k ? 1 : 0, all ? 1 : 0, keep_last ? 1 : 0, keep, kept_tokens, err);
 }
 
 }  // namespace up

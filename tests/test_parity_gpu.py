@@ -178,6 +178,19 @@ def test_bad_cu_seqlens_sets_device_error():
     assert up.get_device_error() == 0x1
 
 
+def test_bad_cu_seqlens_single_sequence():
+    """One sequence whose cu_seqlens disagrees with k's length: the scoring
+    kernel (which starts from the host's sizes for one sequence) checks the
+    bounds itself and loads nothing; the plan reports the error.  q_last holds
+    only the rows the given cu_seqlens implies."""
+    k = torch.zeros(1000, 1, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(3, 1, 64, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 3], dtype=torch.int32, device="cuda")  # total should be 1000
+    up.score_blocks(q, k, cu, 128, 64)
+    torch.cuda.synchronize()
+    assert up.get_device_error() == 0x1
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads (the shapes the benchmark times)
 # ---------------------------------------------------------------------------
@@ -193,6 +206,14 @@ def test_full_size_workloads(name, gain):
     inp = synth.make_workload(name, gain=gain)
     rep = full_check(inp, w["n"], w["G"], w["p"])
     print(name, gain, rep)
+
+
+def test_d256_several_units_per_cta():
+    """head_dim 256 at 700K tokens: the chunk choice gives 304 units for 152 SMs,
+    so every CTA walks two units (the K ring, the Q buffer and the TMEM buffers
+    carry over between them, with the per-panel K turnover of head_dim 256)."""
+    inp = synth.make_inputs([700000], 8, 1, 256, 128, 0.05, gain=5.0, hidden=64, seed=71)
+    full_check(inp, 128, 64, 0.99)
 
 
 def test_full_size_d256_sweep():
