@@ -19,7 +19,8 @@ import torch
 
 from . import _build
 
-__all__ = ["build", "lib", "UpError", "score_blocks_workspace", "score_blocks", "select_topp",
+__all__ = ["build", "lib", "UpError", "score_blocks_workspace", "score_blocks", "shard_heads",
+           "tp_score_blocks", "select_topp",
            "compact_workspace", "compact", "compact_noalloc", "set_kernel_timing_events", "get_device_error", "Sparsifier", "SELECT_MAX_BLOCKS"]
 
 SELECT_MAX_BLOCKS = 16384
@@ -53,6 +54,8 @@ def lib():
     L.up_score_blocks_workspace.restype = SZ
     L.up_score_blocks.argtypes = [P, P, P, I, I64, I, I, I, I, I, P, P, P, SZ, P]
     L.up_score_blocks.restype = I
+    L.up_score_blocks_shard.argtypes = [P, P, P, I, I64, I, I, I, I, I, I, P, P, P, SZ, P]
+    L.up_score_blocks_shard.restype = I
     L.up_select_topp.argtypes = [P, P, P, I, I, ctypes.c_double, P, P, P]
     L.up_select_topp.restype = I
     L.up_select_blocks.argtypes = [P, P, P, I, I, I, ctypes.c_double, I, ctypes.c_uint32, P, P, P]
@@ -110,8 +113,12 @@ def score_blocks_workspace(num_seqs, total_tokens, Hq, Hk, d, n, G) -> int:
 
 
 def score_blocks(q_last, k, cu_seqlens, n, G, scores=None, cu_blocks=None, workspace=None,
-                 stream=None):
-    """Block scores (fp32 [sum nb_s]) and cu_blocks (int32 [B+1]); see up_score_blocks."""
+                 stream=None, Hq_total=None):
+    """Block scores (fp32 [sum nb_s]) and cu_blocks (int32 [B+1]); see up_score_blocks.
+
+    With Hq_total (the query heads of all tensor-parallel ranks), q_last and k
+    hold one rank's heads and the mean over heads divides by Hq_total
+    (up_score_blocks_shard): the shards' scores sum to the scores of all heads."""
     _need(k, "k", torch.bfloat16)
     dev = k.device
     _need(q_last, "q_last", torch.bfloat16, dev)
@@ -131,10 +138,46 @@ def score_blocks(q_last, k, cu_seqlens, n, G, scores=None, cu_blocks=None, works
     ws_need = score_blocks_workspace(B, total, Hq, Hk, d, n, G)
     if workspace is None:
         workspace = _alloc_ws(ws_need, dev)
-    st = lib().up_score_blocks(_ptr(q_last), _ptr(k), _ptr(cu_seqlens), B, total, Hq, Hk, d, n,
-                               G, _ptr(scores), _ptr(cu_blocks), _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _stream(stream))
-    _check("up_score_blocks", st)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if Hq_total is None:
+        st = lib().up_score_blocks(_ptr(q_last), _ptr(k), _ptr(cu_seqlens), B, total, Hq, Hk, d,
+                                   n, G, _ptr(scores), _ptr(cu_blocks), _ptr(workspace), ws_bytes,
+                                   _stream(stream))
+        _check("up_score_blocks", st)
+    else:
+        st = lib().up_score_blocks_shard(_ptr(q_last), _ptr(k), _ptr(cu_seqlens), B, total, Hq,
+                                         Hk, d, n, G, int(Hq_total), _ptr(scores),
+                                         _ptr(cu_blocks), _ptr(workspace), ws_bytes,
+                                         _stream(stream))
+        _check("up_score_blocks_shard", st)
+    return scores, cu_blocks
+
+
+def shard_heads(q_last, k, rank, world):
+    """This rank's tensor-parallel shard: KV heads [r*Hk/W, (r+1)*Hk/W) and the
+    query heads of their GQA groups (views of q_last [rows, Hq, d] and k
+    [tokens, Hk, d], made contiguous).  Hk must divide by the world size."""
+    Hq, Hk = q_last.shape[1], k.shape[1]
+    if Hk % world != 0:
+        raise ValueError(f"{Hk} KV heads do not split over {world} ranks")
+    hk = Hk // world
+    g = Hq // Hk
+    q = q_last[:, rank * hk * g:(rank + 1) * hk * g].contiguous()
+    kk = k[:, rank * hk:(rank + 1) * hk].contiguous()
+    return q, kk
+
+
+def tp_score_blocks(q_last_shard, k_shard, cu_seqlens, n, G, Hq_total, group=None, stream=None):
+    """Tensor-parallel block scores: this rank scores its head shard with the mean
+    over all Hq_total query heads (up_score_blocks_shard), then a sum all-reduce
+    over the process group gives every rank the scores of all heads (UniPrefill
+    overview, fused-kernel paragraph).  Returns (scores, cu_blocks) as
+    score_blocks; every rank then selects on identical scores."""
+    import torch.distributed as dist
+    scores, cu_blocks = score_blocks(q_last_shard, k_shard, cu_seqlens, n, G, stream=stream,
+                                     Hq_total=Hq_total)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+        dist.all_reduce(scores, op=dist.ReduceOp.SUM, group=group)
     return scores, cu_blocks
 
 

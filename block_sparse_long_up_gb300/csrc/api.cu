@@ -182,10 +182,10 @@ size_t up_score_blocks_workspace(int num_seqs, int64_t total_tokens, int Hq, int
     return score_layout(num_seqs, total_tokens, Hq, Hk, d, n, G, up::kChunkQuantum).total;
 }
 
-up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_seqlens,
-                          int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
-                          int G, float *scores, int32_t *cu_blocks, void *workspace,
-                          size_t workspace_bytes, up_stream_t stream) {
+static up_status score_impl(const void *q_last, const void *k, const int32_t *cu_seqlens,
+                            int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
+                            int G, int Hq_norm, float *scores, int32_t *cu_blocks,
+                            void *workspace, size_t workspace_bytes, up_stream_t stream) {
     up_status st = check_score_args(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n,
                                     G, scores, cu_blocks);
     if (st != UP_OK) return st;
@@ -213,6 +213,7 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     p.flag_cap = (int)(32 * lay.max_units + 16);
     p.num_seqs = num_seqs;
     p.Hq = Hq; p.Hk = Hk; p.g = Hq / Hk; p.d = d; p.n = n; p.G = G; p.C = lay.chunk;
+    p.Hq_norm = Hq_norm;
     p.tpt = up::tokens_per_tile(p.g);
     p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
     p.err = ds->err;
@@ -239,6 +240,23 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
     if (up::launch_score_finish(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_finalize(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     return UP_OK;
+}
+
+up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_seqlens,
+                          int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
+                          int G, float *scores, int32_t *cu_blocks, void *workspace,
+                          size_t workspace_bytes, up_stream_t stream) {
+    return score_impl(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n, G, Hq,
+                      scores, cu_blocks, workspace, workspace_bytes, stream);
+}
+
+up_status up_score_blocks_shard(const void *q_last, const void *k, const int32_t *cu_seqlens,
+                                int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
+                                int G, int Hq_total, float *scores, int32_t *cu_blocks,
+                                void *workspace, size_t workspace_bytes, up_stream_t stream) {
+    if (Hq_total < Hq || Hq_total < 1) return UP_ERR_INVALID_ARG;
+    return score_impl(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n, G, Hq_total,
+                      scores, cu_blocks, workspace, workspace_bytes, stream);
 }
 
 up_status up_select_topp(const float *scores, const int32_t *cu_blocks,

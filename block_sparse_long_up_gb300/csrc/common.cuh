@@ -123,6 +123,7 @@ struct ScoreParams {
     int max_units;
     int flag_cap;        // capacity of flag_list
     int num_seqs, Hq, Hk, g, d, n, G, C;
+    int Hq_norm;       // heads the mean over heads divides by (Hq, or all ranks' heads)
     int tpt;           // tokens_per_tile(g)
     float scale_log2;  // log2(e) / sqrt(d)
     unsigned int *err;

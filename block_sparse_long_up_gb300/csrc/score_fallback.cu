@@ -13,7 +13,8 @@
 //
 // Rows.  Per row r of a sequence, over its key chunks c:
 //     m_r = max_c mref[c][r],  l_r = sum_c lsum[c][r] * 2^(mref[c][r] - m_r),
-//     inv_r = 1 / (l_r * n_s * Hq)   (the softmax normaliser and the query/head mean)
+//     inv_r = 1 / (l_r * n_s * Hq_norm)   (the softmax normaliser and the query/head
+//                                         mean; Hq_norm = Hq unless the heads are sharded)
 // and then, in place of mref[c][r], the weight of chunk c's partial sums:
 //     w[c][r] = 2^(mref[c][r] - m_r) * inv_r.
 // With an empty queue every CTA goes straight to the rows; otherwise the CTA
@@ -114,7 +115,8 @@ __device__ __forceinline__ void finalize_rows(const ScoreParams &p, int64_t tota
                          __ldcg(ls[h] + (int64_t)c * R[h]));
             sm[wid][lane + 32 * h] = m[h];
             sl[wid][lane + 32 * h] = l[h];
-            if (wid == 0) sR[lane + 32 * h] = R[h];
+            // the mean over heads divides by n_s * Hq_norm (R = n_s * Hq)
+            if (wid == 0) sR[lane + 32 * h] = R[h] / p.Hq * p.Hq_norm;
         }
         __syncthreads();
         if (wid < 2) {

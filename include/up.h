@@ -105,6 +105,29 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
                           size_t workspace_bytes, up_stream_t stream);
 
 /*
+ * Block scores of one tensor-parallel shard of the heads.
+ *
+ * Source: UniPrefill overview, fused-kernel paragraph: under tensor
+ * parallelism each rank scores the heads it holds and the block scores are
+ * summed across ranks (an all-reduce) before the selection.
+ *
+ * Exactly up_score_blocks for the Hq query / Hk KV heads this rank holds
+ * (q_last [sum n_s, Hq, d], k [total_tokens, Hk, d], whole GQA groups), except
+ * that the mean over heads divides by Hq_total, the query heads of all ranks:
+ * score_b = sum over this shard's rows of the block's softmax mass, divided by
+ * n_s * Hq_total.  The sum of these scores over a partition of all heads into
+ * shards is the up_score_blocks score of all heads (up to fp32 rounding); each
+ * shard's scores sum to Hq / Hq_total per sequence.  Hq_total == Hq gives
+ * up_score_blocks bit for bit.  Same workspace (up_score_blocks_workspace with
+ * this shard's Hq, Hk), outputs and errors as up_score_blocks, plus
+ * UP_ERR_INVALID_ARG for Hq_total < Hq.
+ */
+up_status up_score_blocks_shard(const void *q_last, const void *k, const int32_t *cu_seqlens,
+                                int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
+                                int G, int Hq_total, float *scores, int32_t *cu_blocks,
+                                void *workspace, size_t workspace_bytes, up_stream_t stream);
+
+/*
  * Top-p block selection.
  *
  * Source: UniPrefill overview, top-p selection paragraph: blocks sorted by

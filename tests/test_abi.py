@@ -84,6 +84,14 @@ def test_score_rejects_bad_arguments(L):
     assert call(ws=_fake(272)) == 3  # workspace not 256-byte aligned
 
 
+def test_score_shard_rejects_too_few_total_heads(L):
+    # Hq_total below the shard's own query heads
+    assert L.up_score_blocks_shard(_fake(), _fake(), _fake(), 1, 4096, 8, 2, 64, 128, 64, 4,
+                                   _fake(), _fake(), _fake(), 1 << 30, None) == 1
+    assert L.up_score_blocks_shard(_fake(), _fake(), _fake(), 1, 4096, 8, 2, 64, 128, 64, 0,
+                                   _fake(), _fake(), _fake(), 1 << 30, None) == 1
+
+
 def test_select_and_compact_reject_bad_arguments(L):
     assert L.up_select_topp(_fake(), _fake(), _fake(), 1, 64, 0.0, _fake(), _fake(), None) == 1
     assert L.up_select_topp(_fake(), _fake(), _fake(), 1, 64, float("nan"), _fake(), _fake(), None) == 1

@@ -216,6 +216,36 @@ def test_d256_several_units_per_cta():
     full_check(inp, 128, 64, 0.99)
 
 
+@pytest.mark.parametrize("world", [2, 4])
+def test_tensor_parallel_shards_sum_to_all_heads(world):
+    """Tensor parallelism simulated on one GPU: each shard of the KV heads (with
+    its query heads) is scored with the mean over all query heads; the shards'
+    scores sum to the scores of all heads (oracle within the score tolerance),
+    each shard's scores sum to its share of the heads per sequence, and
+    Hq_total == Hq reproduces score_blocks bit for bit."""
+    Hq, Hk, d, n, G = 32, 8, 128, 128, 64
+    inp = synth.make_inputs([6000, 2500], Hq, Hk, d, n, 0.05, gain=5.0, hidden=64, seed=29)
+    q, k, cu = to_dev_bf16(inp.q_last), to_dev_bf16(inp.k), to_dev_i32(inp.cu_seqlens)
+    nb = int(((np.diff(inp.cu_seqlens) + G - 1) // G).sum())
+    total = np.zeros(nb)
+    for r in range(world):
+        qs, ks = up.shard_heads(q, k, r, world)
+        sc, cb = up.score_blocks(qs, ks, cu, n, G, Hq_total=Hq)
+        torch.cuda.synchronize()
+        part = sc[:nb].cpu().numpy().astype(np.float64)
+        cbn = cb.cpu().numpy()
+        for s in range(inp.num_seqs):
+            assert abs(part[cbn[s]:cbn[s + 1]].sum() - 1.0 / world) <= 1e-4
+        total += part
+    orc_sc, orc_cb = oracle.score_blocks(inp.q_last, inp.k, inp.cu_seqlens, Hq, Hk, d, n, G)
+    nbad, worst = score_failures(total, orc_sc)
+    assert nbad == 0, (nbad, worst)
+    full, _ = up.score_blocks(q, k, cu, n, G)
+    same, _ = up.score_blocks(q, k, cu, n, G, Hq_total=Hq)
+    torch.cuda.synchronize()
+    assert torch.equal(full[:nb], same[:nb])
+
+
 def test_full_size_d256_sweep():
     name = "gqa16x2_d256_128k_sweep"
     w = synth.WORKLOADS[name]
