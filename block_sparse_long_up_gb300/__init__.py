@@ -19,7 +19,8 @@ import torch
 
 from . import _build
 
-__all__ = ["build", "lib", "UpError", "score_blocks_workspace", "score_blocks", "shard_heads",
+__all__ = ["build", "lib", "UpError", "score_blocks_workspace", "score_blocks",
+           "score_blocks_paged", "block_csr", "shard_heads",
            "tp_score_blocks", "select_topp",
            "compact_workspace", "compact", "compact_noalloc", "set_kernel_timing_events", "get_device_error", "Sparsifier", "SELECT_MAX_BLOCKS"]
 
@@ -56,6 +57,11 @@ def lib():
     L.up_score_blocks.restype = I
     L.up_score_blocks_shard.argtypes = [P, P, P, I, I64, I, I, I, I, I, I, P, P, P, SZ, P]
     L.up_score_blocks_shard.restype = I
+    L.up_score_blocks_paged.argtypes = [P, P, I64, I, P, I, P, I, I64, I, I, I, I, I, P, P, P,
+                                        SZ, P]
+    L.up_score_blocks_paged.restype = I
+    L.up_block_csr.argtypes = [P, P, I, P, P, P]
+    L.up_block_csr.restype = I
     L.up_select_topp.argtypes = [P, P, P, I, I, ctypes.c_double, P, P, P]
     L.up_select_topp.restype = I
     L.up_select_blocks.argtypes = [P, P, P, I, I, I, ctypes.c_double, I, ctypes.c_uint32, P, P, P]
@@ -151,6 +157,63 @@ def score_blocks(q_last, k, cu_seqlens, n, G, scores=None, cu_blocks=None, works
                                          _stream(stream))
         _check("up_score_blocks_shard", st)
     return scores, cu_blocks
+
+
+def score_blocks_paged(q_last, k_pages, block_table, cu_seqlens, total_tokens, n, G,
+                       scores=None, cu_blocks=None, workspace=None, stream=None):
+    """Block scores with the keys in a paged cache (chunked prefill); see
+    up_score_blocks_paged.  k_pages bf16 [num_pages, Hk, page_size, d];
+    block_table int32 [num_seqs, max_pages] (key t of sequence s is row
+    t % page_size of page block_table[s, t // page_size]); total_tokens = the
+    sum of the sequence lengths (cu_seqlens[-1])."""
+    _need(k_pages, "k_pages", torch.bfloat16)
+    dev = k_pages.device
+    _need(q_last, "q_last", torch.bfloat16, dev)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    num_pages, Hk, page_size, d = k_pages.shape
+    Hq = q_last.shape[1]
+    B = cu_seqlens.numel() - 1
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [num_seqs, max_pages]")
+    total = int(total_tokens)
+    cap = total // G + B
+    if scores is None:
+        scores = torch.empty(max(cap, 1), dtype=torch.float32, device=dev)
+    if cu_blocks is None:
+        cu_blocks = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    _need(scores, "scores", torch.float32, dev)
+    _need(cu_blocks, "cu_blocks", torch.int32, dev)
+    if scores.numel() < cap:
+        raise ValueError(f"scores needs {cap} entries")
+    if workspace is None:
+        workspace = _alloc_ws(score_blocks_workspace(B, total, Hq, Hk, d, n, G), dev)
+    st = lib().up_score_blocks_paged(_ptr(q_last), _ptr(k_pages), num_pages, page_size,
+                                     _ptr(block_table), block_table.shape[1], _ptr(cu_seqlens), B,
+                                     total, Hq, Hk, d, n, G, _ptr(scores), _ptr(cu_blocks),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream))
+    _check("up_score_blocks_paged", st)
+    return scores, cu_blocks
+
+
+def block_csr(keep, cu_blocks, indptr=None, indices=None, stream=None):
+    """The kept blocks as a block-CSR matrix (indptr int32 [B+1], indices int32
+    [sum nb_s] capacity; entries indptr[s]..indptr[s+1]-1 are sequence s's kept
+    block numbers, ascending); see up_block_csr."""
+    _need(keep, "keep", torch.uint8)
+    dev = keep.device
+    _need(cu_blocks, "cu_blocks", torch.int32, dev)
+    B = cu_blocks.numel() - 1
+    if indptr is None:
+        indptr = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    if indices is None:
+        indices = torch.empty(max(keep.numel(), 1), dtype=torch.int32, device=dev)
+    _need(indptr, "indptr", torch.int32, dev)
+    _need(indices, "indices", torch.int32, dev)
+    _check("up_block_csr", lib().up_block_csr(_ptr(keep), _ptr(cu_blocks), B, _ptr(indptr),
+                                               _ptr(indices), _stream(stream)))
+    return indptr, indices
 
 
 def shard_heads(q_last, k, rank, world):

@@ -182,10 +182,19 @@ size_t up_score_blocks_workspace(int num_seqs, int64_t total_tokens, int Hq, int
     return score_layout(num_seqs, total_tokens, Hq, Hk, d, n, G, up::kChunkQuantum).total;
 }
 
+// Keys in a paged cache (see up_score_blocks_paged); block_table == nullptr:
+// token-major keys.
+struct PagedKeys {
+    const int32_t *block_table;
+    int page_size, max_pages;
+    int64_t num_pages;
+};
+
 static up_status score_impl(const void *q_last, const void *k, const int32_t *cu_seqlens,
                             int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
-                            int G, int Hq_norm, float *scores, int32_t *cu_blocks,
-                            void *workspace, size_t workspace_bytes, up_stream_t stream) {
+                            int G, int Hq_norm, const PagedKeys &pk, float *scores,
+                            int32_t *cu_blocks, void *workspace, size_t workspace_bytes,
+                            up_stream_t stream) {
     up_status st = check_score_args(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n,
                                     G, scores, cu_blocks);
     if (st != UP_OK) return st;
@@ -214,6 +223,10 @@ static up_status score_impl(const void *q_last, const void *k, const int32_t *cu
     p.num_seqs = num_seqs;
     p.Hq = Hq; p.Hk = Hk; p.g = Hq / Hk; p.d = d; p.n = n; p.G = G; p.C = lay.chunk;
     p.Hq_norm = Hq_norm;
+    p.block_table = pk.block_table;
+    p.page_size = pk.page_size;
+    p.max_pages = pk.max_pages;
+    p.num_pages = pk.num_pages;
     p.tpt = up::tokens_per_tile(p.g);
     p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
     p.err = ds->err;
@@ -247,7 +260,7 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
                           int G, float *scores, int32_t *cu_blocks, void *workspace,
                           size_t workspace_bytes, up_stream_t stream) {
     return score_impl(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n, G, Hq,
-                      scores, cu_blocks, workspace, workspace_bytes, stream);
+                      PagedKeys{}, scores, cu_blocks, workspace, workspace_bytes, stream);
 }
 
 up_status up_score_blocks_shard(const void *q_last, const void *k, const int32_t *cu_seqlens,
@@ -256,7 +269,25 @@ up_status up_score_blocks_shard(const void *q_last, const void *k, const int32_t
                                 void *workspace, size_t workspace_bytes, up_stream_t stream) {
     if (Hq_total < Hq || Hq_total < 1) return UP_ERR_INVALID_ARG;
     return score_impl(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n, G, Hq_total,
-                      scores, cu_blocks, workspace, workspace_bytes, stream);
+                      PagedKeys{}, scores, cu_blocks, workspace, workspace_bytes, stream);
+}
+
+up_status up_score_blocks_paged(const void *q_last, const void *k_pages, int64_t num_pages,
+                                int page_size, const int32_t *block_table, int max_pages,
+                                const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens,
+                                int Hq, int Hk, int d, int n, int G, float *scores,
+                                int32_t *cu_blocks, void *workspace, size_t workspace_bytes,
+                                up_stream_t stream) {
+    if (!block_table || page_size < 128 || page_size % 128 != 0 || num_pages < 1 ||
+        max_pages < 1 || Hk < 1 || num_pages * (int64_t)Hk * page_size >= ((int64_t)1 << 31))
+        return UP_ERR_INVALID_ARG;
+    // one sequence starts without the plan's checks: its table row must hold
+    // total_tokens keys (the only valid length)
+    if (num_seqs == 1 && (total_tokens + page_size - 1) / page_size > max_pages)
+        return UP_ERR_INVALID_ARG;
+    const PagedKeys pk{block_table, page_size, max_pages, num_pages};
+    return score_impl(q_last, k_pages, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n, G, Hq,
+                      pk, scores, cu_blocks, workspace, workspace_bytes, stream);
 }
 
 up_status up_select_topp(const float *scores, const int32_t *cu_blocks,
@@ -297,6 +328,18 @@ up_status up_select_blocks(const float *scores, const int32_t *cu_blocks,
     if (up::launch_select(scores, cu_blocks, cu_seqlens, num_seqs, G, mode == UP_SELECT_TOP_K, p,
                           k, (flags & UP_SELECT_KEEP_LAST) != 0, keep, kept_tokens, ds->err, ds->sms,
                           reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return UP_ERR_CUDA;
+    return UP_OK;
+}
+
+up_status up_block_csr(const uint8_t *keep, const int32_t *cu_blocks, int num_seqs,
+                       int32_t *indptr, int32_t *indices, up_stream_t stream) {
+    if (num_seqs < 0 || !keep || !cu_blocks || !indptr || !indices) return UP_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    up_status st = device_state(&ds);
+    if (st != UP_OK) return st;
+    if (up::launch_block_csr(keep, cu_blocks, num_seqs, indptr, indices,
+                             reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return UP_ERR_CUDA;
     return UP_OK;
 }

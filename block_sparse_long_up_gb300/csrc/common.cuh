@@ -124,6 +124,12 @@ struct ScoreParams {
     int flag_cap;        // capacity of flag_list
     int num_seqs, Hq, Hk, g, d, n, G, C;
     int Hq_norm;       // heads the mean over heads divides by (Hq, or all ranks' heads)
+    // Paged keys (null block_table: k is token-major [total, Hk, d]).  Key t of
+    // sequence s is row t % page_size of head j in page block_table[s*max_pages +
+    // t/page_size] of k viewed as [num_pages][Hk][page_size][d].
+    const int32_t *block_table;
+    int page_size, max_pages;
+    int64_t num_pages;
     int tpt;           // tokens_per_tile(g)
     float scale_log2;  // log2(e) / sqrt(d)
     unsigned int *err;
@@ -136,6 +142,18 @@ __device__ __forceinline__ int find_seq_by_unit(const SeqInfo *seqs, int B, int 
         if (seqs[mid].unit_off <= u) lo = mid; else hi = mid - 1;
     }
     return lo;
+}
+
+// Row of key `tok` of sequence s, KV head j, in the paged keys viewed as a 2-D
+// [num_pages * Hk * page_size, d] array; a page index outside [0, num_pages)
+// sets UP_DEVERR_BAD_PAGE and returns the row count (one past the last row).
+__device__ __forceinline__ int64_t paged_row(const ScoreParams &p, int s, int j, int tok) {
+    const int64_t pg = p.block_table[(int64_t)s * p.max_pages + tok / p.page_size];
+    if (pg < 0 || pg >= p.num_pages) {
+        atomicOr(p.err, 0x8u);  // UP_DEVERR_BAD_PAGE
+        return p.num_pages * p.Hk * p.page_size;
+    }
+    return (pg * p.Hk + j) * p.page_size + tok % p.page_size;
 }
 
 // Host-side launchers (each returns the launch's cudaError_t).
@@ -172,5 +190,7 @@ struct CompactArgs {
     int64_t vec_per_row;  // hidden * 2 / 16
 };
 cudaError_t launch_compact(const CompactArgs &a, int num_sms, cudaStream_t st);
+cudaError_t launch_block_csr(const uint8_t *keep, const int32_t *cu_blocks, int num_seqs,
+                             int32_t *indptr, int32_t *indices, cudaStream_t st);
 
 }  // namespace up

@@ -8,6 +8,8 @@
 //                   (source row, destination row, rows), cu_seqlens_out, total;
 //   gather (persistent grid) one work item = up to rows_per_item rows of one
 //                   kept block, copied with 16-byte vector loads and stores.
+// Also here: the kept blocks as a block-CSR matrix for a sparse-attention
+// consumer (FlashPrefill V2 review, key-terms section), by the same scan.
 #include "common.cuh"
 
 namespace up {
@@ -132,12 +134,62 @@ compact_gather_kernel(CompactArgs a) {
     }
 }
 
+// Block CSR of the kept blocks (one CTA): thread t takes a contiguous run of
+// blocks and counts its kept ones, one block-wide scan gives each run's first
+// output slot (kept in shared memory), and each thread writes its kept block
+// numbers.  indptr[s] is the slot of the sequence's first block: the run that
+// holds it plus the kept blocks of that run before it.
+__global__ void __launch_bounds__(kIndexThreads)
+block_csr_kernel(const uint8_t *__restrict__ keep, const int32_t *__restrict__ cu_blocks,
+                 int B, int32_t *__restrict__ indptr, int32_t *__restrict__ indices) {
+    pdl_wait();
+    __shared__ int64_t sh[32];
+    __shared__ int start[kIndexThreads];
+    const int nbt = cu_blocks[B];
+    const int per = (nbt + kIndexThreads - 1) / kIndexThreads;
+    const int g0 = min((int)threadIdx.x * per, nbt), g1 = min(g0 + per, nbt);
+    int cnt = 0;
+    for (int gb = g0; gb < g1; ++gb) cnt += keep[gb] != 0;
+    int64_t tot;
+    const int first = (int)block_excl_scan_i64(cnt, &tot, sh);
+    start[threadIdx.x] = first;
+    if (g0 < g1) {
+        int lo = 0, hi = B - 1;  // the sequence holding g0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cu_blocks[mid] <= g0) lo = mid; else hi = mid - 1;
+        }
+        int pos = first;
+        for (int gb = g0, s = lo; gb < g1; ++gb) {
+            while (cu_blocks[s + 1] <= gb) ++s;
+            if (keep[gb]) indices[pos++] = gb - cu_blocks[s];
+        }
+    }
+    __syncthreads();
+    for (int s = threadIdx.x; s <= B; s += kIndexThreads) {
+        const int b = cu_blocks[s];
+        int v = (int)tot;
+        if (b < nbt) {
+            const int u = b / per;  // the run holding block b
+            v = start[u];
+            for (int gb = u * per; gb < b; ++gb) v += keep[gb] != 0;
+        }
+        indptr[s] = v;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_compact(const CompactArgs &a, int num_sms, cudaStream_t st) {
     cudaError_t e = launch_pdl(compact_index_kernel, dim3(1), dim3(kIndexThreads), 0, st, a);
     if (e != cudaSuccess) return e;
     return launch_pdl(compact_gather_kernel, dim3(num_sms * 4), dim3(kGatherThreads), 0, st, a);
+}
+
+cudaError_t launch_block_csr(const uint8_t *keep, const int32_t *cu_blocks, int num_seqs,
+                             int32_t *indptr, int32_t *indices, cudaStream_t st) {
+    return launch_pdl(block_csr_kernel, dim3(1), dim3(kIndexThreads), 0, st, keep, cu_blocks,
+                      num_seqs, indptr, indices);
 }
 
 }  // namespace up

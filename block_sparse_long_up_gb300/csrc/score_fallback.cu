@@ -200,9 +200,18 @@ score_finish_kernel(ScoreParams p) {
                 __syncthreads();
                 for (int idx = tid; idx < kKeyTile * D; idx += kRowsPerTile) {
                     const int key = kt + idx / D;
-                    ks[idx] = key < k1 ? __bfloat162float(
-                                             p.k[((int64_t)(sq.tok_off + key) * p.Hk + j) * D + idx % D])
-                                       : 0.f;
+                    float v = 0.f;
+                    if (key < k1) {
+                        if (!p.block_table) {
+                            v = __bfloat162float(
+                                p.k[((int64_t)(sq.tok_off + key) * p.Hk + j) * D + idx % D]);
+                        } else {
+                            const int64_t row = paged_row(p, s, j, key);
+                            if (row < p.num_pages * p.Hk * p.page_size)
+                                v = __bfloat162float(p.k[row * D + idx % D]);
+                        }
+                    }
+                    ks[idx] = v;
                 }
                 __syncthreads();
                 tile_logits<D>(qT, ks, tid, acc);

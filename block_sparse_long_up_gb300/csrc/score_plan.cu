@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_blocks,
                   SeqInfo *__restrict__ seqs, Counters *__restrict__ cnt, int B,
                   int64_t total_tokens, int Hq, int Hk, int d, int n, int G, int C,
-                  unsigned int *err) {
+                  int page_size, int max_pages, unsigned int *err) {
     pdl_wait();
     pdl_trigger();  // after the wait: every kernel before this one is complete
     const int lane = threadIdx.x;
@@ -53,6 +53,10 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
         if (s == 0 && v != 0) bad = 1;
         if (s > 0 && v < cu[s - 1]) bad = 1;
         if (s == B && (int64_t)v != total_tokens) bad = 1;
+        // paged keys: every sequence fits its block-table row
+        if (s > 0 && page_size > 0 && v >= cu[s - 1] &&
+            (int64_t)(v - cu[s - 1] + page_size - 1) / page_size > max_pages)
+            bad = 1;
     }
     if (__any_sync(0xffffffffu, bad)) {
         // leave a well-formed empty plan: every later kernel sees no work
@@ -249,7 +253,8 @@ cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, con
                               int64_t total_tokens, cudaStream_t st) {
     return launch_pdl(score_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, cu_seqlens, cu_blocks,
                       const_cast<SeqInfo *>(p.seqs), const_cast<Counters *>(p.counters),
-                      p.num_seqs, total_tokens, p.Hq, p.Hk, p.d, p.n, p.G, p.C, p.err);
+                      p.num_seqs, total_tokens, p.Hq, p.Hk, p.d, p.n, p.G, p.C,
+                      p.block_table ? p.page_size : 0, p.max_pages, p.err);
 }
 
 cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, int num_sms,

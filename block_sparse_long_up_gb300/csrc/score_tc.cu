@@ -95,6 +95,7 @@ struct Shared {
 
 struct Unit {
     SeqInfo sq;
+    int s;  // sequence index
     int j, grp, c, k0, k1, nsteps;
     int npairs;  // pairs of row tiles holding at least one query (a prefix of the pairs)
 };
@@ -103,9 +104,11 @@ template <int D>
 __device__ __forceinline__ void decode_unit(const ScoreParams &p, int u, Unit &un) {
     using C = Cfg<D>;
     if (p.num_seqs == 1) {
+        un.s = 0;
         un.sq = p.seq0;
     } else {
-        un.sq = p.seqs[find_seq_by_unit(p.seqs, p.num_seqs, u)];
+        un.s = find_seq_by_unit(p.seqs, p.num_seqs, u);
+        un.sq = p.seqs[un.s];
     }
     int loc = u - un.sq.unit_off;
     un.grp = loc % un.sq.mtiles;  // group of row tiles
@@ -152,14 +155,22 @@ __device__ void role_tma_k(const CUtensorMap *tmap, const ScoreParams &p, Shared
         Unit un;
         decode_unit<D>(p, u, un);
         for (int t = 0; t < un.nsteps; ++t) {
-            const int row0 = un.sq.tok_off + un.k0 + t * kStepKeys;
+            // the step's 128 keys: rows of k as [tokens, Hk*d] (x = head's dims),
+            // or of the paged keys as [pages*Hk*page_size, d] (a step never
+            // straddles two pages)
+            const int tok = un.k0 + t * kStepKeys;
+            int x0 = un.j * D, row0 = un.sq.tok_off + tok;
+            if (p.block_table) {
+                x0 = 0;
+                row0 = (int)paged_row(p, un.s, un.j, tok);
+            }
             for (int pn = 0; pn < C::kPanels; ++pn, ++it) {
                 const int st = it % C::kStages;
                 const uint32_t ph = (it / C::kStages) & 1;
                 if (!mbar_wait(smem_u32(&sh.kempty[st]), ph ^ 1, abort, kWaitLimit)) goto done;
                 mbar_arrive_expect_tx(smem_u32(&sh.kfull[st]), kPanelBytesK);
-                tma_load_2d_hint(smem_u32(kbuf + st * kPanelBytesK), tmap, un.j * D + pn * 64,
-                                 row0, smem_u32(&sh.kfull[st]), policy);
+                tma_load_2d_hint(smem_u32(kbuf + st * kPanelBytesK), tmap, x0 + pn * 64, row0,
+                                 smem_u32(&sh.kfull[st]), policy);
             }
         }
     }
@@ -693,14 +704,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// K viewed as a 2-D row-major matrix [total_tokens, Hk*d]; one box = 128 rows
-// (keys) x 64 columns (head dims) with the 128-byte swizzle.  Rows past the end
-// read as zeros.
+// K viewed as a 2-D row-major matrix [total_tokens, Hk*d] (paged keys:
+// [num_pages*Hk*page_size, d]); one box = 128 rows (keys) x 64 columns (head
+// dims) with the 128-byte swizzle.  Rows past the end read as zeros.
 bool encode_k_map(CUtensorMap *tm, const ScoreParams &p, int64_t total_tokens) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)p.Hk * p.d, (cuuint64_t)total_tokens};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.Hk * p.d * 2};
+    // paged keys: [num_pages * Hk * page_size rows, d], the same 128 x 64 box
+    const bool paged = p.block_table != nullptr;
+    const cuuint64_t dims[2] = {
+        (cuuint64_t)(paged ? p.d : p.Hk * p.d),
+        (cuuint64_t)(paged ? p.num_pages * p.Hk * p.page_size : total_tokens)};
+    const cuuint64_t strides[1] = {(cuuint64_t)(paged ? p.d : p.Hk * p.d) * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)kStepKeys};
     const cuuint32_t estr[2] = {1, 1};
     return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(p.k), dims,

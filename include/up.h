@@ -59,6 +59,7 @@ typedef enum {
 #define UP_DEVERR_BAD_CU_SEQLENS 0x1u  /* cu_seqlens[0] != 0, decreasing, or last != total_tokens */
 #define UP_DEVERR_SELECT_TOO_MANY_BLOCKS 0x2u /* a sequence has more than UP_SELECT_MAX_BLOCKS blocks */
 #define UP_DEVERR_TIMEOUT 0x4u         /* a bounded wait inside a kernel gave up */
+#define UP_DEVERR_BAD_PAGE 0x8u        /* a page index outside [0, num_pages) (read as zeros) */
 
 /* Largest nb_s that up_select_topp sorts on chip (1M tokens at G = 64). */
 #define UP_SELECT_MAX_BLOCKS 16384
@@ -126,6 +127,57 @@ up_status up_score_blocks_shard(const void *q_last, const void *k, const int32_t
                                 int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
                                 int G, int Hq_total, float *scores, int32_t *cu_blocks,
                                 void *workspace, size_t workspace_bytes, up_stream_t stream);
+
+/*
+ * Block scores with the keys in a paged KV cache (chunked prefill).
+ *
+ * Sources: Chunked Prefill glossary, how-chunking-works section (a long prompt
+ * is prefilled in chunks and each chunk attends to the cached keys of the
+ * earlier ones); CompactAttention review, key-terms section (paged attention
+ * over a KV-head-major cache).
+ *
+ * Exactly up_score_blocks, except where the keys are read: key t of sequence s
+ * (0 <= t < L_s) is row t % page_size of KV head j in page
+ * block_table[s * max_pages + t / page_size] of
+ *   k_pages   bf16 [num_pages, Hk, page_size, d]  (KV-head-major pages).
+ * The query rows of a chunk are its last n_s tokens, as for up_score_blocks,
+ * and a sequence's keys are all of its cached tokens, earlier chunks first.
+ *   block_table  int32 [num_seqs * max_pages]; entries past a sequence's pages
+ *                are not read.
+ *   page_size    a multiple of 128 (a 128-key step never straddles two pages).
+ * Errors: as up_score_blocks; UP_ERR_INVALID_ARG for a null table, page_size
+ * not a positive multiple of 128, num_pages < 1, num_pages * Hk * page_size
+ * >= 2^31, or max_pages < 1; a sequence with more than max_pages * page_size
+ * tokens sets UP_DEVERR_BAD_CU_SEQLENS (nothing is scored); a page index
+ * outside [0, num_pages) sets UP_DEVERR_BAD_PAGE and its keys read as zeros.
+ * The workspace is up_score_blocks_workspace's.
+ */
+up_status up_score_blocks_paged(const void *q_last, const void *k_pages, int64_t num_pages,
+                                int page_size, const int32_t *block_table, int max_pages,
+                                const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens,
+                                int Hq, int Hk, int d, int n, int G, float *scores,
+                                int32_t *cu_blocks, void *workspace, size_t workspace_bytes,
+                                up_stream_t stream);
+
+/*
+ * The kept blocks as a block-CSR matrix (sequences x key blocks) for a
+ * block-sparse attention consumer.
+ *
+ * Source: FlashPrefill V2 review, key-terms section (the active blocks are
+ * handed to the sparse-attention kernel as a CSR index).
+ *
+ *   keep, cu_blocks  as produced by up_select_topp / up_select_blocks and
+ *                    up_score_blocks (cu_blocks int32 [num_seqs+1]).
+ *   indptr   int32 [num_seqs+1] (output): indptr[s] = kept blocks of the
+ *            sequences before s; indptr[num_seqs] = all kept blocks.
+ *   indices  int32 [sum nb_s] (output, capacity): entries indptr[s] ..
+ *            indptr[s+1]-1 are the kept block numbers of sequence s (0-based
+ *            within the sequence), ascending.
+ * One CTA; no workspace.  Errors: UP_ERR_INVALID_ARG for a null pointer or
+ * num_seqs < 0.
+ */
+up_status up_block_csr(const uint8_t *keep, const int32_t *cu_blocks, int num_seqs,
+                       int32_t *indptr, int32_t *indices, up_stream_t stream);
 
 /*
  * Top-p block selection.

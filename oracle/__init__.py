@@ -58,6 +58,8 @@ def _load():
             lib.orc_keep_last_block.restype = i32
             lib.orc_compact.argtypes = [P, P, i64, P, i32, i32, P, P, P, P, P, P]
             lib.orc_compact.restype = i64
+            lib.orc_block_csr.argtypes = [P, P, i32, P, P]
+            lib.orc_block_csr.restype = i64
             _lib = lib
     return _lib
 
@@ -186,3 +188,17 @@ def compact(x, pos, cu_seqlens, G, keep, cu_blocks, with_x=True):
     if got != total_kept:
         raise ValueError("orc_compact rejected its arguments")
     return x_out, pos_out, cu_out, src
+
+
+def block_csr(keep, cu_blocks):
+    """Block CSR of the kept blocks.  Returns (indptr int32 [B+1], indices int32 [nnz])."""
+    lib = _load()
+    keep = _c(keep, np.uint8)
+    cb = _c(cu_blocks, np.int32)
+    B = cb.shape[0] - 1
+    indptr = np.zeros(B + 1, dtype=np.int32)
+    indices = np.zeros(max(int(cb[-1]), 1), dtype=np.int32)
+    nnz = lib.orc_block_csr(_ptr(keep), _ptr(cb), B, _ptr(indptr), _ptr(indices))
+    if nnz < 0:
+        raise ValueError("orc_block_csr rejected its arguments")
+    return indptr, indices[:nnz]

@@ -336,3 +336,22 @@ int64_t orc_compact(const uint16_t *x, const int32_t *pos, int64_t hidden,
     }
     return o;
 }
+
+/* Kept blocks as a block-CSR matrix (FlashPrefill V2 review, key-terms
+ * section: the active blocks handed to a sparse-attention kernel as a CSR
+ * index).  The plain definition: for each sequence in order, the numbers
+ * (0-based within the sequence) of its kept blocks, ascending; indptr[s] =
+ * kept blocks of the sequences before s.  Returns the number of kept blocks,
+ * or -1 for bad arguments. */
+int64_t orc_block_csr(const uint8_t *keep, const int32_t *cu_blocks, int B, int32_t *indptr,
+                      int32_t *indices) {
+    if (B < 0 || !cu_blocks || !indptr) return -1;
+    int64_t nnz = 0;
+    for (int s = 0; s < B; ++s) {
+        indptr[s] = (int32_t)nnz;
+        for (int32_t b = cu_blocks[s]; b < cu_blocks[s + 1]; ++b)
+            if (keep[b]) indices[nnz++] = b - cu_blocks[s];
+    }
+    indptr[B] = (int32_t)nnz;
+    return nnz;
+}

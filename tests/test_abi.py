@@ -92,6 +92,28 @@ def test_score_shard_rejects_too_few_total_heads(L):
                                    _fake(), _fake(), _fake(), 1 << 30, None) == 1
 
 
+def test_score_paged_rejects_bad_arguments(L):
+    def call(pages=64, page=128, table=_fake(), maxp=8, B=2, T=4096):
+        return L.up_score_blocks_paged(_fake(), _fake(), pages, page, table, maxp, _fake(), B, T,
+                                       8, 2, 64, 128, 64, _fake(), _fake(), _fake(), 1 << 30, None)
+
+    assert call(table=None) == 1
+    assert call(page=64) == 1           # not a multiple of 128
+    assert call(page=200) == 1
+    assert call(pages=0) == 1
+    assert call(maxp=0) == 1
+    assert call(pages=1 << 22, page=1024) == 1   # rows past 2^31
+    assert call(B=1, T=4096, maxp=31) == 1       # one sequence longer than its table row
+
+
+def test_block_csr_rejects_bad_arguments(L):
+    assert L.up_block_csr(None, _fake(), 1, _fake(), _fake(), None) == 1
+    assert L.up_block_csr(_fake(), None, 1, _fake(), _fake(), None) == 1
+    assert L.up_block_csr(_fake(), _fake(), 1, None, _fake(), None) == 1
+    assert L.up_block_csr(_fake(), _fake(), 1, _fake(), None, None) == 1
+    assert L.up_block_csr(_fake(), _fake(), -1, _fake(), _fake(), None) == 1
+
+
 def test_select_and_compact_reject_bad_arguments(L):
     assert L.up_select_topp(_fake(), _fake(), _fake(), 1, 64, 0.0, _fake(), _fake(), None) == 1
     assert L.up_select_topp(_fake(), _fake(), _fake(), 1, 64, float("nan"), _fake(), _fake(), None) == 1

@@ -246,6 +246,90 @@ def test_tensor_parallel_shards_sum_to_all_heads(world):
     assert torch.equal(full[:nb], same[:nb])
 
 
+def _paged(inp, page, spare, rng):
+    """The token-major keys of a batch cut into pages of `page` tokens at shuffled
+    page ids of a pool with `spare` extra pages (filled with other bf16 values);
+    unused slots of a sequence's last page hold other values too.
+    Returns (k_pages uint16 [P, Hk, page, d], block_table int32 [B, max_pages])."""
+    lens = np.diff(inp.cu_seqlens)
+    npg = [(int(L) + page - 1) // page for L in lens]
+    P = sum(npg) + spare
+    Hk, d = inp.Hk, inp.d
+    pool = synth.f32_to_bf16_bits(rng.standard_normal((P, Hk, page, d)).astype(np.float32) * 3)
+    ids = rng.permutation(P)
+    maxp = max(max(npg), 1) + 1
+    table = np.full((len(lens), maxp), -1, np.int32)
+    nxt = 0
+    for s, L in enumerate(lens):
+        t0 = int(inp.cu_seqlens[s])
+        for i in range(npg[s]):
+            pg = int(ids[nxt]); nxt += 1
+            table[s, i] = pg
+            a, b = i * page, min((i + 1) * page, int(L))
+            pool[pg, :, : b - a, :] = inp.k[t0 + a:t0 + b].transpose(1, 0, 2)
+    return pool, table
+
+
+@pytest.mark.parametrize("lens,Hq,Hk,d,page", [
+    ([5000], 32, 8, 128, 128),
+    ([3000, 0, 1000, 700], 8, 2, 64, 256),
+    ([4100], 16, 2, 256, 128),
+    ([640, 9000], 32, 8, 128, 384),
+])
+def test_paged_keys_match_token_major(lens, Hq, Hk, d, page):
+    """Keys in a paged, KV-head-major cache (chunked prefill): the scores equal
+    those of the same keys laid out token-major bit for bit (same chunks, same
+    MMAs; masked slots past a sequence's end hold other values), and the
+    oracle's within the tolerance."""
+    rng = np.random.default_rng(sum(lens) + page)
+    inp = synth.make_inputs(lens, Hq, Hk, d, 128, 0.05, gain=5.0, hidden=64, seed=sum(lens) + 5)
+    pool, table = _paged(inp, page, 3, rng)
+    q, k, cu = to_dev_bf16(inp.q_last), to_dev_bf16(inp.k), to_dev_i32(inp.cu_seqlens)
+    G = 64
+    ref, ref_cb = up.score_blocks(q, k, cu, 128, G)
+    sc, cb = up.score_blocks_paged(q, to_dev_bf16(pool), torch.from_numpy(table).cuda(), cu,
+                                   inp.total_tokens, 128, G)
+    torch.cuda.synchronize()
+    nb = int(ref_cb[-1].item())
+    assert torch.equal(cb, ref_cb)
+    assert torch.equal(sc[:nb], ref[:nb])
+    orc_sc, _ = oracle.score_blocks(inp.q_last, inp.k, inp.cu_seqlens, Hq, Hk, d, 128, G)
+    nbad, worst = score_failures(sc[:nb].cpu().numpy().astype(np.float64), orc_sc)
+    assert nbad == 0, (nbad, worst)
+
+
+def test_paged_keys_bad_page_reads_zeros():
+    """A block-table entry past the pool: the error bit is set and that page's
+    keys read as zeros (the tensor map bounds the load; nothing faults)."""
+    rng = np.random.default_rng(3)
+    inp = synth.make_inputs([1000], 8, 2, 64, 32, 0.05, gain=5.0, hidden=64, seed=8)
+    pool, table = _paged(inp, 128, 0, rng)
+    table[0, 2] = pool.shape[0] + 7
+    q, cu = to_dev_bf16(inp.q_last), to_dev_i32(inp.cu_seqlens)
+    up.score_blocks_paged(q, to_dev_bf16(pool), torch.from_numpy(table).cuda(), cu,
+                          inp.total_tokens, 32, 64)
+    torch.cuda.synchronize()
+    assert up.get_device_error() == 0x8
+
+
+@pytest.mark.parametrize("nbs", [[0], [5], [3, 0, 7, 1], [2048], [1000, 0, 2500, 700, 1],
+                                 [6272], [300] * 40])
+def test_block_csr_matches_oracle(nbs):
+    """Block CSR of random keep flags, bit-exact against the oracle: empty
+    sequences, fewer blocks than threads, and several blocks per thread."""
+    rng = np.random.default_rng(sum(nbs) + len(nbs))
+    cb = np.concatenate([[0], np.cumsum(nbs)]).astype(np.int32)
+    for frac in (0.0, 0.03, 0.5, 1.0):
+        keep = (rng.random(int(cb[-1])) < frac).astype(np.uint8)
+        o_ptr, o_idx = oracle.block_csr(keep, cb)
+        k_dev = torch.from_numpy(np.concatenate([keep, np.zeros(1, np.uint8)])).cuda()
+        ptr, idx = up.block_csr(k_dev, to_dev_i32(cb))
+        torch.cuda.synchronize()
+        ptr = ptr.cpu().numpy()
+        np.testing.assert_array_equal(ptr, o_ptr)
+        np.testing.assert_array_equal(idx.cpu().numpy()[: ptr[-1]], o_idx)
+
+
 def test_full_size_d256_sweep():
     name = "gqa16x2_d256_128k_sweep"
     w = synth.WORKLOADS[name]
@@ -298,6 +382,15 @@ def test_overflowing_unit_takes_the_exact_fallback():
     g_sc = sc[: int(orc_cb[-1])].cpu().numpy().astype(np.float64)
     nbad, worst = score_failures(g_sc, orc_sc)
     assert nbad == 0, (nbad, worst)
+    assert up.get_device_error() == 0
+    # the same keys in a paged cache: the fallback reads them through the block table
+    pool, table = _paged(inp, 256, 2, np.random.default_rng(4))
+    ws.zero_()
+    psc, _ = up.score_blocks_paged(q, to_dev_bf16(pool), torch.from_numpy(table).cuda(), cu,
+                                   32768, 128, 64, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws[256 + 16:256 + 20].view(torch.int32).item()) > 0
+    assert torch.equal(psc[: int(orc_cb[-1])], sc[: int(orc_cb[-1])])
     assert up.get_device_error() == 0
 
 
