@@ -168,20 +168,6 @@ up_status check_score_args(const void *q_last, const void *k, const int32_t *cu_
     return UP_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t up_score_blocks_workspace(int num_seqs, int64_t total_tokens, int Hq, int Hk, int d,
-                                 int n, int G) {
-    if (check_score_args(reinterpret_cast<const void *>(16), reinterpret_cast<const void *>(16),
-                         reinterpret_cast<const int32_t *>(16), num_seqs, total_tokens, Hq, Hk,
-                         d, n, G, reinterpret_cast<const float *>(16),
-                         reinterpret_cast<const int32_t *>(16)) != UP_OK)
-        return 0;
-    return score_layout(num_seqs, total_tokens, Hq, Hk, d, n, G, up::kChunkQuantum).total;
-}
-
 // Keys in a paged cache (see up_score_blocks_paged); block_table == nullptr:
 // token-major keys.
 struct PagedKeys {
@@ -190,11 +176,13 @@ struct PagedKeys {
     int64_t num_pages;
 };
 
-static up_status score_impl(const void *q_last, const void *k, const int32_t *cu_seqlens,
-                            int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
-                            int G, int Hq_norm, const PagedKeys &pk, float *scores,
-                            int32_t *cu_blocks, void *workspace, size_t workspace_bytes,
-                            up_stream_t stream) {
+// The scoring call: plan, tensor-core kernel, finish, block sums.  Hq_norm is
+// the head count the mean over heads divides by (Hq, or all tensor-parallel
+// ranks' heads); pk describes paged keys (none: token-major k).
+up_status score_impl(const void *q_last, const void *k, const int32_t *cu_seqlens,
+                     int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n, int G,
+                     int Hq_norm, const PagedKeys &pk, float *scores, int32_t *cu_blocks,
+                     void *workspace, size_t workspace_bytes, up_stream_t stream) {
     up_status st = check_score_args(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n,
                                     G, scores, cu_blocks);
     if (st != UP_OK) return st;
@@ -253,6 +241,20 @@ static up_status score_impl(const void *q_last, const void *k, const int32_t *cu
     if (up::launch_score_finish(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_finalize(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     return UP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t up_score_blocks_workspace(int num_seqs, int64_t total_tokens, int Hq, int Hk, int d,
+                                 int n, int G) {
+    if (check_score_args(reinterpret_cast<const void *>(16), reinterpret_cast<const void *>(16),
+                         reinterpret_cast<const int32_t *>(16), num_seqs, total_tokens, Hq, Hk,
+                         d, n, G, reinterpret_cast<const float *>(16),
+                         reinterpret_cast<const int32_t *>(16)) != UP_OK)
+        return 0;
+    return score_layout(num_seqs, total_tokens, Hq, Hk, d, n, G, up::kChunkQuantum).total;
 }
 
 up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_seqlens,
