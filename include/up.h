@@ -26,8 +26,9 @@
  *     [num_seqs + 1], the exclusive prefix sum of nb_s.
  *   - Host-checkable arguments are validated before any launch; a rejected
  *     call launches nothing and returns the error.  Errors found on the device
- *     (a malformed cu_seqlens, a sequence beyond a kernel's size limit, an
- *     expired bounded wait) set a sticky device error word that
+ *     (a malformed cu_seqlens, a sequence beyond a kernel's size limit, a
+ *     page index outside the key pool, an expired bounded wait) set a sticky
+ *     device error word that
  *     up_get_device_error() reports; the affected outputs are then unspecified.
  *   - Functions are thread-safe; the first call on a device queries its
  *     attributes and sets kernel attributes for it.
@@ -61,7 +62,7 @@ typedef enum {
 #define UP_DEVERR_TIMEOUT 0x4u         /* a bounded wait inside a kernel gave up */
 #define UP_DEVERR_BAD_PAGE 0x8u        /* a page index outside [0, num_pages) (read as zeros) */
 
-/* Largest nb_s that up_select_topp sorts on chip (1M tokens at G = 64). */
+/* Largest nb_s that the selection calls rank on chip (1M tokens at G = 64). */
 #define UP_SELECT_MAX_BLOCKS 16384
 
 /* Static text for a status code. */
@@ -304,8 +305,9 @@ up_status up_compact_noalloc(const void *x, const int32_t *pos, int hidden,
                              int32_t *total_kept, up_stream_t stream);
 
 /*
- * Instrumentation: when both events are non-NULL, every later up_score_blocks
- * call made by this host thread records `start_event` immediately before its
+ * Instrumentation: when both events are non-NULL, every later scoring call
+ * (up_score_blocks, up_score_blocks_shard, up_score_blocks_paged) made by this
+ * host thread records `start_event` immediately before its
  * tensor-core scoring kernel and `stop_event` immediately after it, on the
  * call's stream, so the caller can time that kernel alone with
  * cudaEventElapsedTime.  Pass NULL, NULL to stop.  The events are cudaEvent_t
