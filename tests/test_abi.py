@@ -27,6 +27,27 @@ def _declared_functions():
     return names
 
 
+def test_header_is_plain_c(tmp_path):
+    """include/up.h compiles as C99 with warnings as errors, and every declared
+    entry point can be named from C (its address taken), so a C caller needs
+    nothing but the header and the shared library."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = sorted(_declared_functions())
+    src = tmp_path / "use_up.c"
+    src.write_text('#include "up.h"\n'
+                   "typedef void (*up_fn)(void);\n"
+                   "up_fn up_entry_points[] = {\n" +
+                   "".join(f"    (up_fn)&{n},\n" for n in names) + "};\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic-errors",
+                        "-I", os.path.join(ROOT, "include"), "-c", str(src),
+                        "-o", str(tmp_path / "use_up.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_exports_every_declared_symbol(L):
     names = _declared_functions()
     assert {"up_score_blocks", "up_select_topp", "up_compact"} <= names
