@@ -171,3 +171,22 @@ def test_python_binding_fails_loudly_without_cuda_tensors(L):
     q = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         up.score_blocks(q, q, torch.zeros(2, dtype=torch.int32), 4, 64)
+
+
+def test_oracle_and_kernels_share_no_code():
+    """The oracle (plain C, test infrastructure) and the CUDA library include
+    nothing from each other, and the product package never imports the oracle:
+    there is no CPU path behind the library's calls."""
+    pkg = os.path.join(ROOT, "block_sparse_long_up_gb300")
+    csrc = os.path.join(pkg, "csrc")
+    for fn in os.listdir(csrc):
+        text = open(os.path.join(csrc, fn)).read()
+        assert "oracle" not in text.lower(), fn
+    for fn in os.listdir(os.path.join(ROOT, "oracle")):
+        if fn.endswith((".c", ".h", ".py")):
+            text = open(os.path.join(ROOT, "oracle", fn)).read()
+            assert "csrc" not in text and "up.h" not in text and "block_sparse_long_up_gb300" not in text, fn
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            text = open(os.path.join(pkg, fn)).read()
+            assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), fn
