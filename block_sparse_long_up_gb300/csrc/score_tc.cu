@@ -17,13 +17,15 @@
 // steps (head_dim 256: one pair per unit).
 // A persistent CTA per SM walks its units; roles are warp-specialised:
 //   warp 0      K producer: TMA loads of 128-key x 64-dim K panels (128-byte
-//               swizzle) into a ring of shared-memory stages;
+//               swizzle) into a ring of shared-memory stages (keys token-major,
+//               or through a block table from a paged KV-head-major cache);
 //   warp 2      Q producer: TMA loads of each pair's Q tiles (one 3-D box of
 //               g heads x 128/g queries x 64 dims per tile and panel);
 //   warps 1, 3  MMA issuers, one per TMEM buffer: S = Q K^T as M=128, N=128
 //               tcgen05.mma chains.  The tensor pipe's issue queue is shallow,
 //               so the bookkeeping of one issuer (barrier waits, commits) runs
-//               while the other one's MMAs keep the pipe busy;
+//               while the other one's MMAs keep the pipe busy (head_dim 256:
+//               each K panel is multiplied and released as soon as it lands);
 //   warps 4-11  two softmax warpgroups; warpgroup e owns tile e of each pair.
 //               Thread = row (TMEM lane).  It reads 32 columns at a time (the
 //               next group's TMEM load in flight while the current one is
