@@ -183,28 +183,35 @@ def profiled_traffic(workload, d, G):
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample(inp, heads, queries, threads, G, p):
+def oracle_sample(inp, heads, queries, threads, G, p, cache=None):
     """Time the fp64 oracle on a sample: the first `heads` query heads (with
     their KV heads) and the last `queries` queries of every sequence, over all
     keys, then top-p and compaction of the result.  Returns (seconds, fraction
-    of the full workload's scoring work)."""
+    of the full workload's scoring work, heads used, queries used).  `cache`
+    (a dict) keeps the sliced inputs of a sample size between calls."""
     import oracle
     g = inp.Hq // inp.Hk
     hs = max(1, min(heads, inp.Hq))
     kv = (hs + g - 1) // g
     hs = min(inp.Hq, kv * g) if hs > g else hs
     nq = max(1, min(queries, inp.n))
-    rows, qsel = [], []
-    off = 0
-    for s in range(inp.num_seqs):
-        L = int(inp.cu_seqlens[s + 1] - inp.cu_seqlens[s])
-        ns = min(inp.n, L)
-        keep_q = min(nq, ns)
-        qsel.append(inp.q_last[off + ns - keep_q: off + ns, :hs])
-        rows.append(keep_q)
-        off += ns
-    q = np.ascontiguousarray(np.concatenate(qsel, axis=0))
-    k = np.ascontiguousarray(inp.k[:, :kv])
+    key = (hs, nq)
+    if cache is not None and key in cache:
+        q, k, rows = cache[key]
+    else:
+        rows, qsel = [], []
+        off = 0
+        for s in range(inp.num_seqs):
+            L = int(inp.cu_seqlens[s + 1] - inp.cu_seqlens[s])
+            ns = min(inp.n, L)
+            keep_q = min(nq, ns)
+            qsel.append(inp.q_last[off + ns - keep_q: off + ns, :hs])
+            rows.append(keep_q)
+            off += ns
+        q = np.ascontiguousarray(np.concatenate(qsel, axis=0))
+        k = np.ascontiguousarray(inp.k[:, :kv])
+        if cache is not None:
+            cache[key] = (q, k, rows)
     t0 = time.perf_counter()
     sc, cb = oracle.score_blocks(q, k, inp.cu_seqlens, hs, kv, inp.d, nq, G, nthreads=threads)
     keep, _, _, _ = oracle.select_topp(sc, cb, inp.cu_seqlens, G, p)
@@ -244,15 +251,21 @@ def run_reference(args, inp, w):
     cores = cpu_cores()
     threads = cores
     budget = 150.0 / max(1, args.steps + args.warmup)  # seconds per step
-    # calibrate on one query of one head
-    dt1, frac1, _, _ = oracle_sample(inp, 1, 1, 1, w["G"], w["p"])
+    cache = {}
+    # calibrate on one query of one head (one thread), select and compact included
+    dt1, frac1, _, _ = oracle_sample(inp, 1, 1, 1, w["G"], w["p"], cache)
     per_row = max(dt1, 1e-4)
-    rows_fit = max(1, int(budget * min(threads, inp.Hq) / per_row))
-    heads = min(inp.Hq, max(1, rows_fit // inp.n))
-    queries = inp.n if heads > 1 else max(1, min(inp.n, rows_fit))
+    # the oracle's threads split the query heads, so `threads` heads cost the time
+    # of one: sample that many heads (or all), then as many queries as fit the
+    # budget, then further heads in whole batches of `threads`
+    heads = min(inp.Hq, threads)
+    queries = max(1, min(inp.n, int(budget / per_row)))
+    if queries == inp.n:
+        batches = max(1, int(budget / (per_row * inp.n)))
+        heads = min(inp.Hq, threads * batches)
     times = []
     for i in range(args.warmup + args.steps):
-        dt, frac, hs, nq = oracle_sample(inp, heads, queries, threads, w["G"], w["p"])
+        dt, frac, hs, nq = oracle_sample(inp, heads, queries, threads, w["G"], w["p"], cache)
         if i >= args.warmup:
             times.append(dt)
     t = sum(times) / len(times)
