@@ -237,8 +237,11 @@ def tp_score_blocks(q_last_shard, k_shard, cu_seqlens, n, G, Hq_total, group=Non
     overview, fused-kernel paragraph).  Returns (scores, cu_blocks) as
     score_blocks; every rank then selects on identical scores."""
     import torch.distributed as dist
-    scores, cu_blocks = score_blocks(q_last_shard, k_shard, cu_seqlens, n, G, stream=stream,
-                                     Hq_total=Hq_total)
+    # capacity past sum nb_s is summed too: start it at zero
+    cap = k_shard.shape[0] // G + cu_seqlens.numel() - 1
+    scores = torch.zeros(max(cap, 1), dtype=torch.float32, device=k_shard.device)
+    scores, cu_blocks = score_blocks(q_last_shard, k_shard, cu_seqlens, n, G, scores=scores,
+                                     stream=stream, Hq_total=Hq_total)
     if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
         dist.all_reduce(scores, op=dist.ReduceOp.SUM, group=group)
     return scores, cu_blocks

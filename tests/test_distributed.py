@@ -81,11 +81,15 @@ def _tp_rank_main(rank, world, port, out):
     q, k = as_bf16(inp.q_last), as_bf16(inp.k)
     cu = torch.from_numpy(inp.cu_seqlens)
 
-    def shard_contract(q_last, k_sh, cu_seqlens, n_, G_, stream=None, Hq_total=None):
-        # up_score_blocks_shard's definition: this shard's heads, mean over Hq_total
+    def shard_contract(q_last, k_sh, cu_seqlens, n_, G_, scores=None, stream=None,
+                       Hq_total=None):
+        # up_score_blocks_shard's definition: this shard's heads, mean over Hq_total,
+        # written into the caller's buffer (whose capacity past sum nb_s stays as given)
         sc, cb = oracle.score_blocks(bits(q_last), bits(k_sh), cu_seqlens.numpy(),
                                      q_last.shape[1], k_sh.shape[1], d, n_, G_)
-        return torch.from_numpy(sc * (q_last.shape[1] / Hq_total)), torch.from_numpy(cb)
+        out = scores.to(torch.float64)
+        out[:len(sc)] = torch.from_numpy(sc * (q_last.shape[1] / Hq_total))
+        return out, torch.from_numpy(cb)
 
     up.score_blocks = shard_contract  # tp_score_blocks calls the module's score_blocks
     qs, ks = up.shard_heads(q, k, rank, world)
@@ -93,7 +97,9 @@ def _tp_rank_main(rank, world, port, out):
     sc, cb = up.tp_score_blocks(qs, ks, cu, n, G, Hq)
     full, fcb = oracle.score_blocks(inp.q_last, inp.k, inp.cu_seqlens, Hq, Hk, d, n, G)
     assert np.array_equal(cb.numpy(), fcb)
-    out[rank] = float(np.max(np.abs(sc.numpy() - full)))
+    nb = len(full)
+    assert float(sc[nb:].abs().sum()) == 0.0  # the zeroed capacity stays zero after the sum
+    out[rank] = float(np.max(np.abs(sc[:nb].numpy() - full)))
     dist.destroy_process_group()
 
 
