@@ -22,7 +22,8 @@ from . import _build
 __all__ = ["build", "lib", "UpError", "score_blocks_workspace", "score_blocks",
            "score_blocks_paged", "block_csr", "shard_heads",
            "tp_score_blocks", "select_topp",
-           "compact_workspace", "compact", "compact_noalloc", "set_kernel_timing_events", "get_device_error", "Sparsifier", "SELECT_MAX_BLOCKS"]
+           "compact_workspace", "compact", "compact_noalloc", "set_kernel_timing_events",
+           "set_wait_limit", "get_device_error", "Sparsifier", "SELECT_MAX_BLOCKS"]
 
 SELECT_MAX_BLOCKS = 16384
 _lib = None
@@ -78,6 +79,8 @@ def lib():
     L.up_get_device_error.restype = I
     L.up_measure_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), P]
     L.up_measure_ex2_rate.restype = I
+    L.up_set_wait_limit.argtypes = [ctypes.c_uint64]
+    L.up_set_wait_limit.restype = I
     _lib = L
     return L
 
@@ -235,15 +238,27 @@ def tp_score_blocks(q_last_shard, k_shard, cu_seqlens, n, G, Hq_total, group=Non
     over all Hq_total query heads (up_score_blocks_shard), then a sum all-reduce
     over the process group gives every rank the scores of all heads (UniPrefill
     overview, fused-kernel paragraph).  Returns (scores, cu_blocks) as
-    score_blocks; every rank then selects on identical scores."""
+    score_blocks; every rank then selects on identical scores.
+
+    Everything (the zero fill, the scoring launches and the all-reduce) is
+    issued on `stream` (default: the current stream), so the three are ordered
+    on one stream whichever stream the caller passes."""
+    import contextlib
+
     import torch.distributed as dist
-    # capacity past sum nb_s is summed too: start it at zero
-    cap = k_shard.shape[0] // G + cu_seqlens.numel() - 1
-    scores = torch.zeros(max(cap, 1), dtype=torch.float32, device=k_shard.device)
-    scores, cu_blocks = score_blocks(q_last_shard, k_shard, cu_seqlens, n, G, scores=scores,
-                                     stream=stream, Hq_total=Hq_total)
-    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
-        dist.all_reduce(scores, op=dist.ReduceOp.SUM, group=group)
+    if k_shard.is_cuda:
+        s = torch.cuda.current_stream(k_shard.device) if stream is None else stream
+        on_stream = torch.cuda.stream(s)
+    else:  # host tensors reach here only with a substituted score_blocks (CPU ranks)
+        s, on_stream = stream, contextlib.nullcontext()
+    with on_stream:
+        # capacity past sum nb_s is summed too: start it at zero
+        cap = k_shard.shape[0] // G + cu_seqlens.numel() - 1
+        scores = torch.zeros(max(cap, 1), dtype=torch.float32, device=k_shard.device)
+        scores, cu_blocks = score_blocks(q_last_shard, k_shard, cu_seqlens, n, G, scores=scores,
+                                         stream=s, Hq_total=Hq_total)
+        if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+            dist.all_reduce(scores, op=dist.ReduceOp.SUM, group=group)
     return scores, cu_blocks
 
 
@@ -340,11 +355,37 @@ def compact_noalloc(x, pos, cu_seqlens, G, keep, cu_blocks, x_out, pos_out, cu_s
                     src_idx, total_kept, stream=None):
     """up_compact without a workspace, for callers that cannot allocate device
     memory: every output buffer must be passed in, and the library's fixed
-    scratch is used instead (see up_compact_noalloc in include/up.h)."""
-    for t, name in ((x, "x"), (x_out, "x_out")):
-        _need(t, name, torch.bfloat16)
+    scratch is used instead (see up_compact_noalloc in include/up.h).  src_idx
+    may be None.  Every tensor's type, dtype and size is checked before its
+    device, so a wrong argument raises before anything reaches the library."""
+    args = [(x, "x", torch.bfloat16), (pos, "pos", torch.int32),
+            (cu_seqlens, "cu_seqlens", torch.int32), (keep, "keep", torch.uint8),
+            (cu_blocks, "cu_blocks", torch.int32), (x_out, "x_out", torch.bfloat16),
+            (pos_out, "pos_out", torch.int32), (cu_seqlens_out, "cu_seqlens_out", torch.int32),
+            (total_kept, "total_kept", torch.int32)]
+    if src_idx is not None:
+        args.append((src_idx, "src_idx", torch.int32))
+    for t, name, dtype in args:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if x.dim() != 2 or x_out.dim() != 2 or x_out.shape[1] != x.shape[1]:
+        raise ValueError("x and x_out must be [rows, hidden] with the same hidden size")
     total, hidden = x.shape
     B = cu_seqlens.numel() - 1
+    nb_cap = total // G + B if G > 0 else 0
+    if B < 0 or cu_blocks.numel() != B + 1 or cu_seqlens_out.numel() < B + 1:
+        raise ValueError("cu_seqlens, cu_blocks and cu_seqlens_out must hold num_seqs + 1 entries")
+    if pos.numel() < total or x_out.shape[0] < total or pos_out.numel() < total:
+        raise ValueError("pos, x_out and pos_out must hold total_tokens rows")
+    if src_idx is not None and src_idx.numel() < total:
+        raise ValueError("src_idx must hold total_tokens entries")
+    if keep.numel() < min(nb_cap, 1) or total_kept.numel() < 1:
+        raise ValueError("keep must hold the block flags and total_kept one entry")
+    dev = x.device
+    for t, name, dtype in args:
+        _need(t, name, dtype, dev)
     st = lib().up_compact_noalloc(_ptr(x), _ptr(pos), hidden, _ptr(cu_seqlens), B, total, G,
                                   _ptr(keep), _ptr(cu_blocks), _ptr(x_out), _ptr(pos_out),
                                   _ptr(cu_seqlens_out), _ptr(src_idx), _ptr(total_kept),
@@ -366,6 +407,14 @@ def measure_ex2_rate(stream=None) -> float:
     v = ctypes.c_double(0.0)
     _check("up_measure_ex2_rate", lib().up_measure_ex2_rate(ctypes.byref(v), _stream(stream)))
     return float(v.value)
+
+
+def set_wait_limit(cycles: int = 0):
+    """Bound, in SM clock cycles, of every spin-wait inside the scoring kernel
+    for scoring calls issued after this one (0: the default, about two
+    seconds).  For tests of the failure path: an expired wait stops the
+    kernel cleanly and sets the timeout bit that get_device_error() reports."""
+    _check("up_set_wait_limit", lib().up_set_wait_limit(int(cycles)))
 
 
 def get_device_error() -> int:
@@ -398,9 +447,12 @@ class Sparsifier:
         self.ws_compact = _alloc_ws(compact_workspace(num_seqs, total_tokens, G), dev)
 
     def launches_per_step(self) -> int:
-        # score: plan, tensor-core main, finish (exact fallback, row statistics), block sums;
-        # select: 1; compact: index, gather
-        return (4 if self.total > 0 and self.num_seqs > 0 else 1) + 1 + 2
+        # score: plan, tensor-core kernel (scores included), finish (the exact
+        # fallback; returns at once unless a tile overflowed); select: 1;
+        # compact: 1, or index + gather past 16384 possible blocks
+        score = 3 if self.total > 0 and self.num_seqs > 0 else 1
+        compact = 1 if self.total // self.G + self.num_seqs <= 16384 else 2
+        return score + 1 + compact
 
     def run(self, q_last, k, cu_seqlens, x, pos, stream=None):
         score_blocks(q_last, k, cu_seqlens, self.n, self.G, self.scores, self.cu_blocks,

@@ -1,5 +1,6 @@
 // api.cu -- the C ABI declared in include/up.h: argument validation, workspace
 // layout, per-device state and kernel launches.  No compute happens here.
+#include <atomic>
 #include <mutex>
 
 #include "../../include/up.h"
@@ -23,6 +24,11 @@ DeviceState g_dev[kMaxDevices];
 // optional events recorded around the tensor-core scoring kernel (per host thread)
 thread_local cudaEvent_t t_kernel_start = nullptr, t_kernel_stop = nullptr;
 
+// Bound of the scoring kernel's spin-waits in SM clock cycles (about two
+// seconds at the GB300's clocks unless a test lowers it).
+constexpr long long kDefaultWaitLimit = 4000000000LL;
+std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+
 up_status device_state(DeviceState **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return UP_ERR_CUDA;
@@ -41,6 +47,17 @@ up_status device_state(DeviceState **out) {
 }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+}  // namespace
+
+namespace up {
+unsigned int *device_error_word() {
+    DeviceState *ds = nullptr;
+    return device_state(&ds) == UP_OK ? ds->err : nullptr;
+}
+}  // namespace up
+
+namespace {
 
 bool valid_G(int G) { return G == 16 || G == 32 || G == 64 || G == 128 || G == 256; }
 bool valid_d(int d) { return d == 64 || d == 128 || d == 256; }
@@ -137,6 +154,12 @@ up_status up_set_kernel_timing_events(up_event_t start_event, up_event_t stop_ev
     return UP_OK;
 }
 
+up_status up_set_wait_limit(uint64_t cycles) {
+    if (cycles > (uint64_t)kDefaultWaitLimit) return UP_ERR_INVALID_ARG;
+    g_wait_limit.store(cycles == 0 ? kDefaultWaitLimit : (long long)cycles);
+    return UP_OK;
+}
+
 up_status up_get_device_error(uint32_t *bits) {
     if (!bits) return UP_ERR_INVALID_ARG;
     DeviceState *ds = nullptr;
@@ -176,7 +199,8 @@ struct PagedKeys {
     int64_t num_pages;
 };
 
-// The scoring call: plan, tensor-core kernel, finish, block sums.  Hq_norm is
+// The scoring call: plan, tensor-core kernel (scores included), finish (only
+// does work when a tile overflowed).  Hq_norm is
 // the head count the mean over heads divides by (Hq, or all tensor-parallel
 // ranks' heads); pk describes paged keys (none: token-major k).
 up_status score_impl(const void *q_last, const void *k, const int32_t *cu_seqlens,
@@ -217,6 +241,7 @@ up_status score_impl(const void *q_last, const void *k, const int32_t *cu_seqlen
     p.num_pages = pk.num_pages;
     p.tpt = up::tokens_per_tile(p.g);
     p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
+    p.wait_limit = g_wait_limit.load();
     p.err = ds->err;
     p.cu_seqlens = cu_seqlens;
     if (num_seqs == 1) {  // the plan's row for the only sequence, from the host's sizes
@@ -239,7 +264,6 @@ up_status score_impl(const void *q_last, const void *k, const int32_t *cu_seqlen
     if (up::launch_score_main(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     if (t_kernel_stop && cudaEventRecord(t_kernel_stop, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_finish(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
-    if (up::launch_score_finalize(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     return UP_OK;
 }
 
@@ -384,6 +408,8 @@ up_status up_compact(const void *x, const int32_t *pos, int hidden, const int32_
     a.nkept = reinterpret_cast<int32_t *>(ws + lay.nkept);
     a.list = reinterpret_cast<int4 *>(ws + lay.list);
     a.dst_blk = reinterpret_cast<int32_t *>(ws + lay.dst_blk);
+    a.err = ds->err;
+    a.max_blocks = total_tokens / G + num_seqs;
     a.num_seqs = num_seqs;
     a.G = G;
     a.hidden = hidden;

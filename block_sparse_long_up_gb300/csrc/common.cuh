@@ -69,7 +69,8 @@ struct Counters {
     int64_t rows;        // sum R_s
     int32_t flagged;     // units queued for the exact fallback
     int32_t fin_done;    // CTAs of the finishing kernel done with the fallback (flagged case)
-    int32_t pad[10];
+    int32_t bar[2];      // the scoring kernel's two grid barriers (CTAs arrived)
+    int32_t pad[8];
 };
 static_assert(sizeof(Counters) == 64, "Counters is 64 bytes");
 
@@ -116,7 +117,8 @@ struct ScoreParams {
     SeqInfo seq0;
     int units0;
     float *part;   // [b][r] per sequence: block partial sums (relative to mref)
-    float *mref;   // [c][r] per sequence: reference (log2 units) of the chunk's partials
+    float *mref;   // [c][r] per sequence: reference (log2 units) of the chunk's partials,
+                   // then (overwritten in place) the weight of the chunk's partials
     float *lsum;   // [c][r] per sequence: sum of the chunk's partials
     float *scores;
     int32_t *flag_list;  // 4*unit + row tile of tiles whose sums overflowed (exact fallback)
@@ -132,6 +134,7 @@ struct ScoreParams {
     int64_t num_pages;
     int tpt;           // tokens_per_tile(g)
     float scale_log2;  // log2(e) / sqrt(d)
+    long long wait_limit;  // bound of every spin-wait of the scoring kernel, SM clock cycles
     unsigned int *err;
 };
 
@@ -161,11 +164,10 @@ cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, con
                               int64_t total_tokens, cudaStream_t st);
 cudaError_t launch_score_main(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
                               cudaStream_t st);
-// the exact fallback for queued tiles, then the row statistics and chunk weights
+// only when tiles overflowed: their exact fallback, then every row's statistics
+// and every block score
 cudaError_t launch_score_finish(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
                                cudaStream_t st);
-cudaError_t launch_score_finalize(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
-                                  cudaStream_t st);
 // top_k: keep the first k ranks (p unused); otherwise top-p with p.
 cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const int32_t *cu_seqlens,
                           int num_seqs, int G, bool top_k, double p, int k, bool keep_last,
@@ -183,13 +185,21 @@ struct CompactArgs {
     int32_t *cu_out;
     int32_t *src_idx;
     int32_t *total_kept;
-    int4 *list;        // workspace: kept blocks (src row, dst row, rows, -)
-    int32_t *nkept;    // workspace: number of kept blocks
-    int32_t *dst_blk;  // workspace: destination row of every block
+    int4 *list;        // scratch (blocks beyond the one-kernel limit): kept blocks (src row, dst row, rows, -)
+    int32_t *nkept;    // scratch: number of kept blocks
+    int32_t *dst_blk;  // scratch: destination row of every block
+    unsigned int *err; // the device error word
+    int64_t max_blocks;  // total_tokens / G + num_seqs: the most blocks the batch can have
     int num_seqs, G, hidden, rows_per_item, items_per_block;
     int64_t vec_per_row;  // hidden * 2 / 16
 };
+// Compaction kernels: one kernel when max_blocks <= kCompactOneKernelBlocks
+// (every CTA scans the keep flags itself; the scratch is not used), else an
+// index kernel that writes the kept-block list to the scratch and a gather.
+constexpr int64_t kCompactOneKernelBlocks = 16384;
 cudaError_t launch_compact(const CompactArgs &a, int num_sms, cudaStream_t st);
+// The device error word of the current device (nullptr if it cannot be looked up).
+unsigned int *device_error_word();
 cudaError_t launch_block_csr(const uint8_t *keep, const int32_t *cu_blocks, int num_seqs,
                              int32_t *indptr, int32_t *indices, cudaStream_t st);
 

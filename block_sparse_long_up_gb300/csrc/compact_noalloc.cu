@@ -13,6 +13,9 @@
 // code holds it (about 1.3 MB) until the process exits.  Host code cannot use
 // the array's name as a device address, so the first call on each device looks
 // the address up with cudaGetSymbolAddress while that device is current.
+// Batches of at most kCompactOneKernelBlocks possible blocks take the
+// one-kernel compaction, which needs no scratch at all; larger ones (up to
+// UP_COMPACT_NOALLOC_MAX_BLOCKS) use the array.
 #include <mutex>
 
 #include "../../include/up.h"
@@ -95,6 +98,11 @@ extern "C" up_status up_compact_noalloc(const void *x, const int32_t *pos, int h
     a.nkept = reinterpret_cast<int32_t *>(dev->scratch);
     a.list = reinterpret_cast<int4 *>(dev->scratch + kCounterBytes);
     a.dst_blk = reinterpret_cast<int32_t *>(dev->scratch + kCounterBytes + kListBytes);
+    // the kernels check cu_blocks[num_seqs] against this bound on the device, so
+    // a cu_blocks that disagrees with total_tokens never reaches past the array
+    a.max_blocks = total_tokens / G + num_seqs;
+    a.err = up::device_error_word();
+    if (!a.err) return UP_ERR_CUDA;
     a.num_seqs = num_seqs;
     a.G = G;
     a.hidden = hidden;

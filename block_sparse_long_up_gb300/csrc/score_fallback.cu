@@ -1,25 +1,27 @@
-// score_fallback.cu -- the kernel that finishes the scoring statistics after
-// the tensor-core kernel: an exact CUDA-core fallback for the rare overflowed
-// tiles, then each softmax row's normaliser and the weights of its chunks.
+// score_fallback.cu -- the exact fallback of block scoring, for the rare row
+// tiles whose fp32 sums overflowed in the tensor-core kernel.
 //
-// Fallback.  The tensor-core kernel measures every partial sum against a
-// reference taken from the first 32 keys of a work unit.  If a later key of the
-// same unit has a logit more than ~115 binary orders of magnitude above that
-// reference, its fp32 sums overflow; the kernel then queues that 128-row tile
-// here.  The tile is recomputed with two passes over the logits: the first
-// finds each row's exact maximum m over the unit's keys (log2 units), the
-// second sums 2^(z*log2e/sqrt(d) - m) over every block.  The queue is empty for
-// ordinary attention logits.
+// The tensor-core kernel measures every partial sum against a reference taken
+// from the first 32 keys of a work unit.  If a later key of the same unit has a
+// logit more than ~115 binary orders of magnitude above that reference, its
+// fp32 sums overflow; the kernel then queues that 128-row tile here (and its
+// own epilogue stops: the scores it would write are replaced below).  The
+// queue is empty for ordinary attention logits, and this kernel then returns
+// at once.
 //
-// Rows.  Per row r of a sequence, over its key chunks c:
+// Tiles.  Each queued tile is recomputed with two passes over the logits: the
+// first finds each row's exact maximum m over the unit's keys (log2 units),
+// the second sums 2^(z*log2e/sqrt(d) - m) over every block.
+//
+// Rows, then blocks (by the CTA that finishes its tiles last, a counter the
+// plan kernel zeroes).  Per row r of a sequence, over its key chunks c:
 //     m_r = max_c mref[c][r],  l_r = sum_c lsum[c][r] * 2^(mref[c][r] - m_r),
 //     inv_r = 1 / (l_r * n_s * Hq_norm)   (the softmax normaliser and the query/head
 //                                         mean; Hq_norm = Hq unless the heads are sharded)
-// and then, in place of mref[c][r], the weight of chunk c's partial sums:
-//     w[c][r] = 2^(mref[c][r] - m_r) * inv_r.
-// With an empty queue every CTA goes straight to the rows; otherwise the CTA
-// that finishes its queued tiles last (a counter the plan kernel zeroes) does
-// all rows after every recomputed tile is in memory.
+// and then, in place of mref[c][r], the weight of chunk c's partial sums,
+//     w[c][r] = 2^(mref[c][r] - m_r) * inv_r;
+// finally score_b = sum_r part[b][r] * w[c(b)][r] in a fixed order.  One CTA
+// does all rows and blocks: slow, but only taken for overflowing inputs.
 // Source: UniPrefill overview, block-wise importance estimation paragraph.
 #include "common.cuh"
 
@@ -146,16 +148,43 @@ __device__ __forceinline__ void finalize_rows(const ScoreParams &p, int64_t tota
     }
 }
 
+// Every block score, by one CTA: thread t sums rows t, t + 128, ... of the
+// block in order, then a fixed butterfly and the warps in order.
+__device__ void finalize_blocks_one_cta(const ScoreParams &p) {
+    __shared__ float red[kRowsPerTile / 32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int nbt = p.counters->blocks;
+    int s = 0;
+    for (int gb = 0; gb < nbt; ++gb) {
+        while (gb >= p.seqs[s].blk_off + p.seqs[s].nb) ++s;  // skips empty sequences
+        const SeqInfo &sq = p.seqs[s];
+        const int b = gb - sq.blk_off;
+        const float *w = p.mref + sq.stat_off + (int64_t)block_slot(b, p.G, p.C) * sq.R;
+        const float *pt = p.part + sq.part_off + (int64_t)b * sq.R;
+        float acc = 0.f;
+        for (int r = threadIdx.x; r < sq.R; r += kRowsPerTile)
+            acc = fmaf(__ldcg(pt + r), __ldcg(w + r), acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) red[wid] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float t = 0.f;
+#pragma unroll
+            for (int k = 0; k < kRowsPerTile / 32; ++k) t += red[k];
+            p.scores[gb] = t;
+        }
+        __syncthreads();
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kRowsPerTile, 4)
 score_finish_kernel(ScoreParams p) {
     pdl_wait();
     const int nflag = min(p.counters->flagged, p.flag_cap);
     const int64_t total_rows = p.counters->rows;
-    if (nflag == 0) {
-        finalize_rows(p, total_rows, blockIdx.x, gridDim.x);
-        return;
-    }
+    if (nflag == 0) return;  // the tensor-core kernel's epilogue wrote the scores
     extern __shared__ __align__(16) unsigned char smem[];
     __nv_bfloat16 *qT = reinterpret_cast<__nv_bfloat16 *>(smem);                 // [D][128]
     float *ks = reinterpret_cast<float *>(smem + D * kRowsPerTile * 2);          // [32][D]
@@ -250,6 +279,9 @@ score_finish_kernel(ScoreParams p) {
     if (s_last) {
         __threadfence();
         finalize_rows(p, total_rows, 0, 1);
+        __threadfence();
+        __syncthreads();
+        finalize_blocks_one_cta(p);
     }
 }
 
@@ -259,11 +291,9 @@ cudaError_t launch_d(const ScoreParams &p, int64_t max_rows, int num_sms, cudaSt
     cudaError_t e = cudaFuncSetAttribute(score_finish_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    // one 64-row pass per CTA for the rows, at least one CTA per SM for the queue
-    const int64_t passes = (max_rows + kRowsPerPass - 1) / kRowsPerPass;
-    const int64_t want = passes > num_sms ? passes : num_sms;
-    const int grid = (int)(want < 65535 ? want : 65535);
-    return launch_pdl(score_finish_kernel<D>, dim3(grid), dim3(kRowsPerTile), smem, st, p);
+    // one CTA per SM for the queue (empty for ordinary inputs: every CTA returns at once)
+    (void)max_rows;
+    return launch_pdl(score_finish_kernel<D>, dim3(num_sms), dim3(kRowsPerTile), smem, st, p);
 }
 
 }  // namespace

@@ -61,7 +61,7 @@ constexpr int kPanelBytesQ = kRowsPerTile * 128;   // 128 rows x 64 bf16 = 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBufCols = 2 * kStepKeys;            // one TMEM buffer: a pair of tiles
 constexpr int kSmemBudget = 227 * 1024 - 2048;     // dynamic bytes we allow ourselves
-constexpr long long kWaitLimit = 4000000000LL;     // cycles, ~2 s
+constexpr long long kWaitLimit = 4000000000LL;     // cycles, ~2 s: the drain after an abort
 constexpr int kMaxStages = 16;
 
 template <int D>
@@ -93,6 +93,7 @@ struct Shared {
     uint32_t tmem_base;
     int units;
     int abort;
+    int epi_state;  // epilogue: 0 go on, 1 a wait expired, 2 tiles overflowed (the finish kernel redoes all)
 };
 
 struct Unit {
@@ -150,7 +151,7 @@ __device__ void role_tma_k(const CUtensorMap *tmap, const ScoreParams &p, Shared
     using C = Cfg<D>;
     volatile int *abort = &sh.abort;
     // K is read exactly once: its lines should leave L2 before the block
-    // partials, which the finalize reads back
+    // partials, which the epilogue reads back
     const uint64_t policy = l2_policy_evict_first();
     uint32_t it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -169,7 +170,7 @@ __device__ void role_tma_k(const CUtensorMap *tmap, const ScoreParams &p, Shared
             for (int pn = 0; pn < C::kPanels; ++pn, ++it) {
                 const int st = it % C::kStages;
                 const uint32_t ph = (it / C::kStages) & 1;
-                if (!mbar_wait(smem_u32(&sh.kempty[st]), ph ^ 1, abort, kWaitLimit)) goto done;
+                if (!mbar_wait(smem_u32(&sh.kempty[st]), ph ^ 1, abort, p.wait_limit)) goto done;
                 mbar_arrive_expect_tx(smem_u32(&sh.kfull[st]), kPanelBytesK);
                 tma_load_2d_hint(smem_u32(kbuf + st * kPanelBytesK), tmap, x0 + pn * 64, row0,
                                  smem_u32(&sh.kfull[st]), policy);
@@ -206,7 +207,7 @@ __device__ void role_tma_q(const CUtensorMap *tmap, const ScoreParams &p, Shared
         decode_unit<D>(p, u, un);
         for (int pr = 0; pr < un.npairs; ++pr) {
             const int qs = (ui % C::kQBufs) * C::kPairs + pr;
-            if (!mbar_wait(smem_u32(&sh.qempty[qs]), ((parity >> qs) & 1u) ^ 1u, abort, kWaitLimit))
+            if (!mbar_wait(smem_u32(&sh.qempty[qs]), ((parity >> qs) & 1u) ^ 1u, abort, p.wait_limit))
                 goto done;
             mbar_arrive_expect_tx(smem_u32(&sh.qfull[qs]), tx);
             for (int e = 0; e < 2; ++e) {
@@ -264,18 +265,18 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
                 // after its MMAs, so a stage is held ~0.3 us instead of a step.
                 if ((gstep & 1u) != (uint32_t)w) continue;  // the other issuer's step
                 if (!q_ready) {
-                    if (!mbar_wait(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort, kWaitLimit))
+                    if (!mbar_wait(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort, p.wait_limit))
                         goto out;
                     q_ready = true;
                 }
-                if (!mbar_wait(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, kWaitLimit))
+                if (!mbar_wait(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, p.wait_limit))
                     goto out;
                 tc_fence_after();
 #pragma unroll 1
                 for (int pn = 0; pn < C::kPanels; ++pn) {
                     const uint32_t i = it0 + pn;
                     const int st = i % C::kStages;
-                    if (!mbar_wait(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort, kWaitLimit))
+                    if (!mbar_wait(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort, p.wait_limit))
                         goto out;
                     tc_fence_after();
                     const uint64_t bd = smem_desc_sw128(smem_u32(kbuf + st * kPanelBytesK));
@@ -305,17 +306,17 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
                 for (int pn = 0; pn < C::kPanels; ++pn) {
                     const uint32_t i = it0 + pn;
                     if (!mbar_wait(smem_u32(&sh.kfull[i % C::kStages]), (i / C::kStages) & 1,
-                                   abort, kWaitLimit))
+                                   abort, p.wait_limit))
                         goto out;
                 }
                 if (pair_ok) {
                     if (!q_ready) {
                         if (!mbar_wait(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort,
-                                       kWaitLimit))
+                                       p.wait_limit))
                             goto out;
                         q_ready = true;
                     }
-                    if (!mbar_wait(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, kWaitLimit))
+                    if (!mbar_wait(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, p.wait_limit))
                         goto out;
                     tc_fence_after();
 #pragma unroll
@@ -382,7 +383,7 @@ __device__ __forceinline__ void mask_group(float (&v)[32], int key, int a) {
 }
 
 // One predicated store (no branch, so the group code stays one basic block),
-// with an L2 evict-last policy: the finalize reads the partials back.
+// with an L2 evict-last policy: the epilogue reads the partials back.
 __device__ __forceinline__ void st_if(float *p, float v, bool ok, uint64_t policy) {
     asm volatile(
         "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
@@ -565,7 +566,7 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
                 if (pr >= un.npairs) break;
                 const int buf = C::kPairs == 2 ? pr : (int)(gstep & 1u);
                 const bool ok = next_ready || mbar_wait(smem_u32(&sh.tfull[buf]),
-                                                        (tpar >> buf) & 1u, abort, kWaitLimit);
+                                                        (tpar >> buf) & 1u, abort, p.wait_limit);
                 next_ready = false;
                 __syncwarp();  // tcgen05.ld is warp-collective: reconverge after polling
                 if (!__all_sync(0xffffffffu, ok)) return;
@@ -617,6 +618,243 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
     }
 }
 
+__device__ __forceinline__ int ld_acquire(const int32_t *ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float dot4(const float4 x, const float4 y, float a) {
+    a = fmaf(x.x, y.x, a);
+    a = fmaf(x.y, y.y, a);
+    a = fmaf(x.z, y.z, a);
+    return fmaf(x.w, y.w, a);
+}
+
+// Grid barrier of the epilogue: every CTA of the grid arrives (its earlier
+// global writes made visible first), then waits for all of them, at most
+// wait_limit cycles (then the timeout bit is set and false returned).  The
+// grid is at most one CTA per SM, so all of its CTAs are resident together
+// unless other work holds SMs for longer than the bound.  Thread 0 also reads
+// the overflow queue counter after the first barrier (every tile that will
+// ever be queued is queued by then).
+__device__ __forceinline__ int grid_barrier(const ScoreParams &p, int32_t *ctr, Shared &sh,
+                                            bool read_flags) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        atomicAdd(ctr, 1);
+        const int n = (int)gridDim.x;
+        bool ok = ld_acquire(ctr) >= n;
+        if (!ok) {
+            const long long t0 = clock64();
+            while (!(ok = ld_acquire(ctr) >= n))
+                if (clock64() - t0 > p.wait_limit) break;
+        }
+        int st = ok ? 0 : 1;
+        if (!ok) atomicOr(p.err, UP_DEVERR_TIMEOUT);
+        if (ok && read_flags &&
+            *reinterpret_cast<const volatile int32_t *>(&p.counters->flagged) > 0)
+            st = 2;
+        sh.epi_state = st;
+    }
+    __syncthreads();
+    return sh.epi_state;
+}
+
+__device__ __forceinline__ int find_seq_by_row(const SeqInfo *seqs, int B, int64_t r) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seqs[mid].row_off <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int find_seq_by_block(const SeqInfo *seqs, int B, int gb) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seqs[mid].blk_off <= gb) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Epilogue, all threads of every CTA, after the CTA's last unit:
+//   barrier 1 -- every unit of the grid is done: all partials and statistics
+//                are in memory (if a tile was queued for the exact fallback,
+//                stop here: the finish kernel redoes the rows and blocks);
+//   rows      -- a contiguous share of all softmax rows per CTA, one row per
+//                thread: over the row's key chunks c (in order, up to
+//                kEpiChunks of them loaded at once), the maximum M and
+//                normaliser l,
+//                  M = max_c mref[c][r],  l = sum_c lsum[c][r] * 2^(mref[c][r] - M),
+//                then, in place of mref[c][r], the weight of chunk c's
+//                partials, w = 2^(mref[c][r] - M) / (l * n_s * Hq_norm);
+//   barrier 2 -- every weight is in memory;
+//   blocks    -- a contiguous share of all blocks per CTA, in batches of up to
+//                kEpiBlocks blocks of one chunk: score_b = sum_r part[b][r] *
+//                w[c(b)][r], thread t taking the float4 groups t, t + 384, ...
+//                of the rows in order, then a fixed butterfly and the warps in
+//                order -- independent of the grid and the batching, so the
+//                scores are bitwise reproducible.
+// Loads of other CTAs' results bypass L1.
+constexpr int kEpiChunks = 24;  // chunk statistics a thread has in flight
+constexpr int kEpiBlocks = 6;   // blocks of one batch (all of their partials in flight)
+constexpr int kEpiVec = 3;      // float4 groups per thread and block in flight (rows <= 4608)
+constexpr int kWarps = kThreads / 32;
+
+// Online merge of a row's (maximum, normaliser) with one chunk's (reference, sum).
+__device__ __forceinline__ void merge_chunk(float &M, float &l, float m, float s) {
+    if (m == -INFINITY) return;
+    if (M == -INFINITY) {
+        M = m;
+        l = s;
+        return;
+    }
+    const float mn = fmaxf(M, m);
+    l = l * exp2f(M - mn) + s * exp2f(m - mn);
+    M = mn;
+}
+
+__device__ void epilogue_rows(const ScoreParams &p) {
+    const int64_t total = p.counters->rows;
+    const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = (int64_t)blockIdx.x * per, r1 = min(r0 + per, total);
+    for (int64_t gr = r0 + threadIdx.x; gr < r1; gr += kThreads) {
+        const SeqInfo &sq = p.num_seqs == 1 ? p.seq0 : p.seqs[find_seq_by_row(p.seqs, p.num_seqs, gr)];
+        const int64_t r = gr - sq.row_off;
+        float *mref = p.mref + sq.stat_off + r;
+        const float *lsum = p.lsum + sq.stat_off + r;
+        const float norm = (float)sq.ns * (float)p.Hq_norm;
+        float M = -INFINITY, l = 0.f;
+        if (sq.nchunks <= kEpiChunks) {
+            // every chunk's statistics in flight at once, kept for the weights
+            float m[kEpiChunks], s[kEpiChunks];
+#pragma unroll
+            for (int k = 0; k < kEpiChunks; ++k) {
+                const bool ok = k < sq.nchunks;
+                m[k] = ok ? __ldcg(mref + (int64_t)k * sq.R) : -INFINITY;
+                s[k] = ok ? __ldcg(lsum + (int64_t)k * sq.R) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < kEpiChunks; ++k) merge_chunk(M, l, m[k], s[k]);
+            const float inv = (M == -INFINITY || !(l > 0.f)) ? 0.f : 1.0f / (l * norm);
+#pragma unroll
+            for (int k = 0; k < kEpiChunks; ++k)
+                if (k < sq.nchunks)
+                    mref[(int64_t)k * sq.R] =
+                        (m[k] == -INFINITY || inv == 0.f) ? 0.f : exp2f(m[k] - M) * inv;
+            continue;
+        }
+        for (int c0 = 0; c0 < sq.nchunks; c0 += kEpiChunks) {
+            float m[kEpiChunks], s[kEpiChunks];
+#pragma unroll
+            for (int k = 0; k < kEpiChunks; ++k) {
+                const bool ok = c0 + k < sq.nchunks;
+                m[k] = ok ? __ldcg(mref + (int64_t)(c0 + k) * sq.R) : -INFINITY;
+                s[k] = ok ? __ldcg(lsum + (int64_t)(c0 + k) * sq.R) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < kEpiChunks; ++k) merge_chunk(M, l, m[k], s[k]);
+        }
+        const float inv = (M == -INFINITY || !(l > 0.f)) ? 0.f : 1.0f / (l * norm);
+        for (int c0 = 0; c0 < sq.nchunks; c0 += kEpiChunks) {
+            float m[kEpiChunks];
+#pragma unroll
+            for (int k = 0; k < kEpiChunks; ++k)
+                m[k] = c0 + k < sq.nchunks ? __ldcg(mref + (int64_t)(c0 + k) * sq.R) : -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kEpiChunks; ++k)
+                if (c0 + k < sq.nchunks)
+                    mref[(int64_t)(c0 + k) * sq.R] =
+                        (m[k] == -INFINITY || inv == 0.f) ? 0.f : exp2f(m[k] - M) * inv;
+        }
+    }
+}
+
+__device__ void epilogue_blocks(const ScoreParams &p, float (*red)[kWarps]) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int nbt = p.counters->blocks;
+    const int per = (nbt + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int lo = (int)blockIdx.x * per, hi = min(lo + per, nbt);
+    if (lo >= hi) return;
+    const int bpc = p.C / p.G;  // blocks per key chunk
+    int s = p.num_seqs == 1 ? 0 : find_seq_by_block(p.seqs, p.num_seqs, lo);
+    for (int gb = lo; gb < hi;) {
+        if (p.num_seqs != 1)
+            while (gb >= p.seqs[s].blk_off + p.seqs[s].nb) ++s;  // skips empty sequences
+        const SeqInfo &sq = p.num_seqs == 1 ? p.seq0 : p.seqs[s];
+        const int b = gb - sq.blk_off;
+        const int nbat = min(min(kEpiBlocks, hi - gb), min(sq.nb - b, (b / bpc + 1) * bpc - b));
+        const float *wr = p.mref + sq.stat_off + (int64_t)block_slot(b, p.G, p.C) * sq.R;
+        const float *pt = p.part + sq.part_off + (int64_t)b * sq.R;
+        float acc[kEpiBlocks];
+#pragma unroll
+        for (int k = 0; k < kEpiBlocks; ++k) acc[k] = 0.f;
+        if ((sq.R % 4 == 0) && ((sq.stat_off | sq.part_off) % 4 == 0)) {
+            const float4 *w4 = reinterpret_cast<const float4 *>(wr);
+            const float4 *p4 = reinterpret_cast<const float4 *>(pt);
+            const int R4 = sq.R / 4;
+            const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i0 = threadIdx.x; i0 < R4; i0 += kEpiVec * kThreads) {
+                float4 w[kEpiVec], x[kEpiBlocks][kEpiVec];
+#pragma unroll
+                for (int u = 0; u < kEpiVec; ++u) {
+                    const int i = i0 + u * kThreads;
+                    w[u] = i < R4 ? __ldcg(w4 + i) : zero;
+                }
+#pragma unroll
+                for (int k = 0; k < kEpiBlocks; ++k)
+#pragma unroll
+                    for (int u = 0; u < kEpiVec; ++u) {
+                        const int i = i0 + u * kThreads;
+                        x[k][u] = (k < nbat && i < R4) ? __ldcg(p4 + (int64_t)k * R4 + i) : zero;
+                    }
+#pragma unroll
+                for (int k = 0; k < kEpiBlocks; ++k)
+#pragma unroll
+                    for (int u = 0; u < kEpiVec; ++u) acc[k] = dot4(x[k][u], w[u], acc[k]);
+            }
+        } else {
+            for (int r = threadIdx.x; r < sq.R; r += kThreads) {
+                const float w = __ldcg(wr + r);
+#pragma unroll
+                for (int k = 0; k < kEpiBlocks; ++k)
+                    if (k < nbat) acc[k] = fmaf(__ldcg(pt + (int64_t)k * sq.R + r), w, acc[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kEpiBlocks; ++k) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < kEpiBlocks; ++k) red[k][wid] = acc[k];
+        }
+        __syncthreads();
+        if ((int)threadIdx.x < nbat) {
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) t += red[threadIdx.x][w];
+            p.scores[gb + threadIdx.x] = t;
+        }
+        __syncthreads();
+        gb += nbat;
+    }
+}
+
+template <int D>
+__device__ void score_epilogue(const ScoreParams &p, Shared &sh, float *smem_f) {
+    pdl_wait();  // the plan's table and counters
+    Counters *cnt = const_cast<Counters *>(p.counters);
+    if (grid_barrier(p, &cnt->bar[0], sh, true) != 0) return;
+    epilogue_rows(p);
+    if (grid_barrier(p, &cnt->bar[1], sh, false) != 0) return;
+    epilogue_blocks(p, reinterpret_cast<float(*)[kWarps]>(smem_f));
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
@@ -655,6 +893,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             mbar_init(smem_u32(&sh.fin[b]), 1);
         }
         sh.abort = 0;
+        sh.epi_state = 0;
         fence_mbar_init();
     }
     if (warp == kWarpMma0) {
@@ -688,6 +927,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    if (!sh.abort) {
+        // the epilogue's generic stores reuse shared memory the TMA wrote
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        score_epilogue<D>(p, sh, reinterpret_cast<float *>(smem));
     }
     if (threadIdx.x == 0 && sh.abort) atomicOr(p.err, UP_DEVERR_TIMEOUT);
     pdl_wait();  // this grid completes after the plan: later kernels read its table

@@ -62,6 +62,7 @@ class Inputs:
     hidden: int
     salient: list           # per-sequence salient fraction
     gain: float | None
+    planted: list = dataclasses.field(default_factory=list)  # per sequence: salient planting blocks
 
     @property
     def total_tokens(self) -> int:
@@ -148,7 +149,7 @@ def make_inputs(lens, Hq, Hk, d, n, salient, gain=5.0, hidden=None, seed=1000,
         x = _normal_bf16(rng_x, (total, hidden))
     pos = np.concatenate([np.arange(L, dtype=np.int32) for L in lens]) if total else np.zeros(0, np.int32)
     return Inputs(q_last=q_last, k=k, cu_seqlens=cu, x=x, pos=pos, Hq=Hq, Hk=Hk, d=d, n=n,
-                  hidden=int(hidden or 0), salient=fracs, gain=gain)
+                  hidden=int(hidden or 0), salient=fracs, gain=gain, planted=plant)
 
 
 # Named workloads (shapes from the long-context prefill setting the pages

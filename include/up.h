@@ -61,6 +61,7 @@ typedef enum {
 #define UP_DEVERR_SELECT_TOO_MANY_BLOCKS 0x2u /* a sequence has more than UP_SELECT_MAX_BLOCKS blocks */
 #define UP_DEVERR_TIMEOUT 0x4u         /* a bounded wait inside a kernel gave up */
 #define UP_DEVERR_BAD_PAGE 0x8u        /* a page index outside [0, num_pages) (read as zeros) */
+#define UP_DEVERR_BAD_CU_BLOCKS 0x10u  /* compaction: cu_blocks[num_seqs] < 0 or > total_tokens/G + num_seqs */
 
 /* Largest nb_s that the selection calls rank on chip (1M tokens at G = 64). */
 #define UP_SELECT_MAX_BLOCKS 16384
@@ -262,7 +263,10 @@ up_status up_select_blocks(const float *scores, const int32_t *cu_blocks,
  *   total_kept      int32 [1] (output): number of kept rows (= cu_seqlens_out[num_seqs]).
  *   workspace       at least up_compact_workspace(...) bytes, 256-byte aligned.
  * The output size lives on the device; reading it on the host is the caller's
- * choice (one device-to-host copy of total_kept).
+ * choice (one device-to-host copy of total_kept).  A cu_blocks whose last entry
+ * is negative or above total_tokens/G + num_seqs (not one that up_score_blocks
+ * wrote for this batch) sets UP_DEVERR_BAD_CU_BLOCKS; nothing is copied and
+ * total_kept is 0.
  */
 size_t up_compact_workspace(int num_seqs, int64_t total_tokens, int G);
 
@@ -325,6 +329,19 @@ up_status up_set_kernel_timing_events(up_event_t start_event, up_event_t stop_ev
  * the method; no page counterpart.
  */
 up_status up_measure_ex2_rate(double *ex2_per_second, up_stream_t stream);
+
+/*
+ * Instrumentation for tests of the failure path: every spin-wait inside the
+ * tensor-core scoring kernel (a role waiting for shared-memory data, a free
+ * TMEM buffer or another CTA's results) gives up after `cycles` SM clock
+ * cycles; the kernel then stops every role of the CTA, lets its copies and
+ * MMAs in flight complete, frees its tensor memory, returns and sets
+ * UP_DEVERR_TIMEOUT (the call's outputs are then unspecified).  0 restores
+ * the default bound (4e9 cycles, about two seconds); a bound above the
+ * default returns UP_ERR_INVALID_ARG.  Process-wide; it applies to scoring
+ * calls issued after it.  Not part of the method; no page counterpart.
+ */
+up_status up_set_wait_limit(uint64_t cycles);
 
 /*
  * Reads and clears the sticky device error word of the current device

@@ -11,6 +11,9 @@ Comparison contract (numbers fixed by the benchmark spec of this library):
 """
 from __future__ import annotations
 
+import logging
+import os
+
 import numpy as np
 import torch
 
@@ -20,6 +23,12 @@ import oracle
 SCORE_RTOL = 1e-3
 SCORE_ATOL = 1e-6
 BAND = 1e-4
+
+# every full_check's report, in order: tests/conftest.py prints them in the
+# terminal summary, so a quiet run still shows the worst score error and the
+# excused kept-set count of each case
+REPORTS: list = []
+log = logging.getLogger("parity")
 
 
 def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
@@ -95,7 +104,9 @@ def full_check(inp, n, G, p, check_x=True, nthreads=None):
                                                     g_cb, inp.cu_seqlens, G, p)
     hard2, _ = keep_mismatch(g_keep, ref_keep, ci2, ce2, p)
     assert hard2 == 0
-    report = dict(excused=excused, worst_rel=worst, kept=int(g_keep.sum()), blocks=len(g_keep))
+    max_abs = float(np.max(np.abs(g_sc - orc_sc))) if len(g_sc) else 0.0
+    report = dict(excused=excused, worst_rel=worst, max_abs=max_abs, kept=int(g_keep.sum()),
+                  blocks=len(g_keep), n=n, G=G, p=p)
     if check_x and inp.x is not None:
         xo, po, cuo, src, T = gpu_compact(inp.x, inp.pos, inp.cu_seqlens, G, g_keep, g_cb)
         ox, opos, ocu, osrc = oracle.compact(inp.x, inp.pos, inp.cu_seqlens, G, g_keep, g_cb)
@@ -105,4 +116,7 @@ def full_check(inp, n, G, p, check_x=True, nthreads=None):
         np.testing.assert_array_equal(po, opos)
         assert np.array_equal(xo, ox)
         report["kept_tokens"] = T
+    report["case"] = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    REPORTS.append(report)
+    log.info("parity %s", report)
     return report

@@ -190,3 +190,51 @@ def test_oracle_and_kernels_share_no_code():
         if fn.endswith(".py"):
             text = open(os.path.join(pkg, fn)).read()
             assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), fn
+
+
+def test_wait_limit_bounds(L):
+    """The failure-path hook takes a bound up to the default and 0 (restore)."""
+    assert L.up_set_wait_limit(ctypes.c_uint64(1 << 62)) == 1
+    assert L.up_set_wait_limit(ctypes.c_uint64(5000)) == 0
+    assert L.up_set_wait_limit(ctypes.c_uint64(0)) == 0
+
+
+def test_compact_noalloc_checks_every_tensor_before_the_library(monkeypatch):
+    """Every argument of the no-workspace compaction is checked in Python
+    (type, dtype, size, then device) before anything reaches the C library: a
+    wrong dtype that would make the kernel read or write out of bounds raises
+    first."""
+    import torch
+
+    def no_library():
+        raise AssertionError("the C library was reached")
+
+    monkeypatch.setattr(up, "lib", no_library)
+    T, H, G, B = 256, 16, 64, 2
+    good = dict(x=torch.zeros(T, H, dtype=torch.bfloat16), pos=torch.zeros(T, dtype=torch.int32),
+                cu_seqlens=torch.tensor([0, 100, T], dtype=torch.int32), G=G,
+                keep=torch.zeros(T // G + B, dtype=torch.uint8),
+                cu_blocks=torch.zeros(B + 1, dtype=torch.int32),
+                x_out=torch.zeros(T, H, dtype=torch.bfloat16),
+                pos_out=torch.zeros(T, dtype=torch.int32),
+                cu_seqlens_out=torch.zeros(B + 1, dtype=torch.int32),
+                src_idx=torch.zeros(T, dtype=torch.int32),
+                total_kept=torch.zeros(1, dtype=torch.int32))
+    wrong_dtype = dict(keep=torch.int64, pos=torch.float32, cu_seqlens=torch.int64,
+                       cu_blocks=torch.int64, x_out=torch.float16, pos_out=torch.int64,
+                       cu_seqlens_out=torch.int16, src_idx=torch.int64, total_kept=torch.int64,
+                       x=torch.float32)
+    for name, dt in wrong_dtype.items():
+        args = dict(good)
+        args[name] = args[name].to(dt)
+        with pytest.raises(TypeError, match=name):
+            up.compact_noalloc(**args)
+    for name, short in (("pos_out", torch.zeros(T - 1, dtype=torch.int32)),
+                        ("src_idx", torch.zeros(T - 1, dtype=torch.int32)),
+                        ("cu_blocks", torch.zeros(B, dtype=torch.int32))):
+        args = dict(good)
+        args[name] = short
+        with pytest.raises(ValueError):
+            up.compact_noalloc(**args)
+    with pytest.raises(ValueError, match="CUDA"):
+        up.compact_noalloc(**good)  # right dtypes and sizes, but host tensors

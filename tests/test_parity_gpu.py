@@ -170,6 +170,53 @@ def test_compact_random_keep(hidden):
         assert np.array_equal(xo, ox)
 
 
+@pytest.mark.parametrize("G,lens,seed", [
+    (16, [200000, 0, 77, 100003], 1),       # up to 18759 blocks: index kernel + gather
+    (64, [3000] * 300 + [1, 5, 70000], 2),  # 303 sequences, up to 15459 blocks: one kernel
+])
+def test_compact_both_paths_large_batches(G, lens, seed):
+    """Batches on both sides of the one-kernel limit (16384 possible blocks):
+    many short sequences and a few long ones, every keep density; bit-exact
+    against the oracle."""
+    rng = np.random.default_rng(seed)
+    cu = np.zeros(len(lens) + 1, np.int32)
+    cu[1:] = np.cumsum(lens)
+    nbs = [(L + G - 1) // G for L in lens]
+    cb = np.zeros(len(lens) + 1, np.int32)
+    cb[1:] = np.cumsum(nbs)
+    hidden = 8
+    x = rng.integers(0, 1 << 16, size=(int(cu[-1]), hidden), dtype=np.uint16)
+    pos = rng.integers(-5, 1 << 30, size=int(cu[-1])).astype(np.int32)
+    for prob in (0.02, 0.5, 1.0):
+        keep = (rng.random(int(cb[-1])) < prob).astype(np.uint8)
+        xo, po, cuo, src, T = gpu_compact(x, pos, cu, G, keep, cb)
+        ox, opos, ocu, osrc = oracle.compact(x, pos, cu, G, keep, cb)
+        assert T == len(opos)
+        np.testing.assert_array_equal(cuo, ocu)
+        np.testing.assert_array_equal(src, osrc)
+        np.testing.assert_array_equal(po, opos)
+        assert np.array_equal(xo, ox)
+
+
+@pytest.mark.parametrize("total", [4096, 2000000])
+def test_compact_rejects_a_block_count_the_batch_cannot_have(total):
+    """cu_blocks whose last entry exceeds total_tokens/G + num_seqs (here: not
+    the cu_blocks of this batch) is caught on the device before any scan or
+    scratch write, on both compaction paths: the error bit is set and nothing
+    is kept."""
+    G = 64
+    x = torch.zeros(total, 8, dtype=torch.bfloat16, device="cuda")
+    pos = torch.zeros(total, dtype=torch.int32, device="cuda")
+    cu = torch.tensor([0, total], dtype=torch.int32, device="cuda")
+    bad_nb = total // G + 5
+    cb = torch.tensor([0, bad_nb], dtype=torch.int32, device="cuda")
+    keep = torch.ones(bad_nb, dtype=torch.uint8, device="cuda")
+    _, _, _, tk, _ = up.compact(x, pos, cu, G, keep, cb)
+    torch.cuda.synchronize()
+    assert int(tk.item()) == 0
+    assert up.get_device_error() == 0x10
+
+
 def test_bad_cu_seqlens_sets_device_error():
     k = torch.zeros(100, 1, 64, dtype=torch.bfloat16, device="cuda")
     q = torch.zeros(10, 1, 64, dtype=torch.bfloat16, device="cuda")
@@ -204,8 +251,7 @@ def test_bad_cu_seqlens_single_sequence():
 def test_full_size_workloads(name, gain):
     w = synth.WORKLOADS[name]
     inp = synth.make_workload(name, gain=gain)
-    rep = full_check(inp, w["n"], w["G"], w["p"])
-    print(name, gain, rep)
+    full_check(inp, w["n"], w["G"], w["p"])
 
 
 def test_d256_several_units_per_cta():
@@ -228,10 +274,15 @@ def test_tensor_parallel_shards_sum_to_all_heads(world):
     q, k, cu = to_dev_bf16(inp.q_last), to_dev_bf16(inp.k), to_dev_i32(inp.cu_seqlens)
     nb = int(((np.diff(inp.cu_seqlens) + G - 1) // G).sum())
     total = np.zeros(nb)
+    cap = inp.total_tokens // G + inp.num_seqs
     for r in range(world):
         qs, ks = up.shard_heads(q, k, r, world)
-        sc, cb = up.score_blocks(qs, ks, cu, n, G, Hq_total=Hq)
+        # a zero-filled buffer as the all-reduce gets it: the shard call writes
+        # only the sum nb_s real entries and leaves the capacity past them at zero
+        sc = torch.zeros(cap + 16, dtype=torch.float32, device="cuda")
+        sc, cb = up.score_blocks(qs, ks, cu, n, G, scores=sc, Hq_total=Hq)
         torch.cuda.synchronize()
+        assert bool((sc[nb:] == 0).all())
         part = sc[:nb].cpu().numpy().astype(np.float64)
         cbn = cb.cpu().numpy()
         for s in range(inp.num_seqs):
@@ -391,6 +442,28 @@ def test_overflowing_unit_takes_the_exact_fallback():
     torch.cuda.synchronize()
     assert int(ws[256 + 16:256 + 20].view(torch.int32).item()) > 0
     assert torch.equal(psc[: int(orc_cb[-1])], sc[: int(orc_cb[-1])])
+    assert up.get_device_error() == 0
+
+
+def test_expired_wait_stops_the_scoring_kernel_cleanly():
+    """Failure detection without a fault: with the spin-wait bound lowered to a
+    few hundred cycles, the scoring kernel's first waits for data run out.
+    The call still returns, every CTA stops (copies and MMAs in flight are
+    drained, tensor memory freed), the timeout bit reaches the host through
+    the device error word, and the next call at the default bound matches the
+    oracle on the same context."""
+    inp = synth.make_inputs([6000, 3000], 8, 2, 128, 128, 0.05, gain=5.0, hidden=64, seed=21)
+    q, k, cu = to_dev_bf16(inp.q_last), to_dev_bf16(inp.k), to_dev_i32(inp.cu_seqlens)
+    assert up.get_device_error() == 0
+    up.set_wait_limit(300)
+    try:
+        up.score_blocks(q, k, cu, 128, 64)
+        torch.cuda.synchronize()
+    finally:
+        up.set_wait_limit(0)
+    bits = up.get_device_error()
+    assert bits & 0x4, f"the timeout bit was not set (bits {bits:#x})"
+    full_check(inp, 128, 64, 0.99)
     assert up.get_device_error() == 0
 
 

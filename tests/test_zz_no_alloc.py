@@ -4,10 +4,11 @@ Such callers (an engine that has already reserved nearly all HBM for its KV
 cache, or a serving loop that must not call cudaMalloc because it can
 synchronise the device) get this entry point, which uses a fixed scratch array
 inside the library instead of a workspace.  These tests call it through the C
-ABI twice in a row, with different batches, and require its outputs to equal
-those of up_compact (compaction is a bit copy, so equal means bit-exact).  The
-second call has fewer kept blocks than the first, so a result built from the
-first call's leftover scratch would show up.
+ABI twice in a row, with different batches large enough to need the scratch,
+and require its outputs to equal those of up_compact (compaction is a bit
+copy, so equal means bit-exact).  The second call has fewer kept blocks than
+the first, so a result built from the first call's leftover scratch would
+show up.
 
 This file is collected last so that a run stopping at its first failure has
 already run every other test.
@@ -72,13 +73,24 @@ def _same_as_up_compact(b):
 
 
 def test_noalloc_matches_up_compact_on_two_calls_in_a_row():
+    """Both batches can hold more blocks than the one-kernel compaction takes
+    (16384), so both calls go through the library's fixed scratch array."""
     assert torch.cuda.is_available()
     up.build()
-    first = _batch([3000, 0, 129, 4096, 77], 64, 4096, 0.6, seed=1)
-    second = _batch([513, 2048, 5], 32, 520, 0.2, seed=2)
+    first = _batch([150000, 0, 129, 140000, 77], 16, 64, 0.6, seed=1)   # up to 18142 blocks
+    second = _batch([513, 280000, 5], 16, 24, 0.2, seed=2)              # up to 17532 blocks
     t1 = _same_as_up_compact(first)
     t2 = _same_as_up_compact(second)
     assert t1 > t2 > 0
+    assert up.get_device_error() == 0
+
+
+def test_noalloc_small_batch():
+    """A batch within the one-kernel limit needs no scratch at all; the entry
+    point gives up_compact's result there too."""
+    up.build()
+    b = _batch([3000, 0, 129, 4096, 77], 64, 4096, 0.6, seed=4)
+    assert _same_as_up_compact(b) > 0
     assert up.get_device_error() == 0
 
 
