@@ -447,10 +447,9 @@ class Sparsifier:
         self.ws_compact = _alloc_ws(compact_workspace(num_seqs, total_tokens, G), dev)
 
     def launches_per_step(self) -> int:
-        # score: plan, tensor-core kernel (scores included), finish (the exact
-        # fallback; returns at once unless a tile overflowed); select: 1;
+        # score: plan, tensor-core kernel (scores included); select: 1;
         # compact: 1, or index + gather past 16384 possible blocks
-        score = 3 if self.total > 0 and self.num_seqs > 0 else 1
+        score = 2 if self.total > 0 and self.num_seqs > 0 else 1
         compact = 1 if self.total // self.G + self.num_seqs <= 16384 else 2
         return score + 1 + compact
 

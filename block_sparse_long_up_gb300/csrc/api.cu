@@ -199,8 +199,7 @@ struct PagedKeys {
     int64_t num_pages;
 };
 
-// The scoring call: plan, tensor-core kernel (scores included), finish (only
-// does work when a tile overflowed).  Hq_norm is
+// The scoring call: plan, then the tensor-core kernel (scores included).  Hq_norm is
 // the head count the mean over heads divides by (Hq, or all tensor-parallel
 // ranks' heads); pk describes paged keys (none: token-major k).
 up_status score_impl(const void *q_last, const void *k, const int32_t *cu_seqlens,
@@ -263,7 +262,6 @@ up_status score_impl(const void *q_last, const void *k, const int32_t *cu_seqlen
     if (t_kernel_start && cudaEventRecord(t_kernel_start, s) != cudaSuccess) return UP_ERR_CUDA;
     if (up::launch_score_main(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     if (t_kernel_stop && cudaEventRecord(t_kernel_stop, s) != cudaSuccess) return UP_ERR_CUDA;
-    if (up::launch_score_finish(p, lay, ds->sms, s) != cudaSuccess) return UP_ERR_CUDA;
     return UP_OK;
 }
 

@@ -67,9 +67,8 @@ struct Counters {
     int32_t units;       // score work units
     int32_t blocks;      // sum nb_s
     int64_t rows;        // sum R_s
-    int32_t flagged;     // units queued for the exact fallback
-    int32_t fin_done;    // CTAs of the finishing kernel done with the fallback (flagged case)
-    int32_t bar[2];      // the scoring kernel's two grid barriers (CTAs arrived)
+    int32_t flagged;     // row tiles queued for the exact fallback
+    int32_t bar[3];      // the scoring kernel's grid barriers (CTAs arrived)
     int32_t pad[8];
 };
 static_assert(sizeof(Counters) == 64, "Counters is 64 bytes");
@@ -164,10 +163,6 @@ cudaError_t launch_score_plan(const int32_t *cu_seqlens, int32_t *cu_blocks, con
                               int64_t total_tokens, cudaStream_t st);
 cudaError_t launch_score_main(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
                               cudaStream_t st);
-// only when tiles overflowed: their exact fallback, then every row's statistics
-// and every block score
-cudaError_t launch_score_finish(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
-                               cudaStream_t st);
 // top_k: keep the first k ranks (p unused); otherwise top-p with p.
 cudaError_t launch_select(const float *scores, const int32_t *cu_blocks, const int32_t *cu_seqlens,
                           int num_seqs, int G, bool top_k, double p, int k, bool keep_last,

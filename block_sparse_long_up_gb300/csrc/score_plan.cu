@@ -5,10 +5,9 @@
 //           count; zeroes the counters of the scoring kernel's grid barriers.
 //   main    (tensor-core kernel, score_tc.cu) per (row, block) partial softmax
 //           sums relative to a per (row, chunk) reference, the chunk's
-//           reference and sum; then, across the whole grid, every row's
+//           reference and sum; then, across the whole grid, the exact
+//           recomputation of any tile whose sums overflowed, every row's
 //           normaliser and chunk weights, and every block score.
-//   finish  (score_fallback.cu) only when a tile's sums overflowed: its exact
-//           recomputation, then every row and every block again.
 // UniPrefill overview, block-wise importance estimation paragraph: the block
 // score is the softmax attention mass of the last n queries that falls into a
 // block, averaged over queries and heads.
@@ -60,8 +59,8 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
         // leave a well-formed empty plan: every later kernel sees no work
         if (lane == 0) {
             atomicOr(err, 0x1u);
-            cnt->units = 0; cnt->blocks = 0; cnt->rows = 0; cnt->flagged = 0; cnt->fin_done = 0;
-            cnt->bar[0] = 0; cnt->bar[1] = 0;
+            cnt->units = 0; cnt->blocks = 0; cnt->rows = 0; cnt->flagged = 0;
+            cnt->bar[0] = 0; cnt->bar[1] = 0; cnt->bar[2] = 0;
         }
         for (int s = lane; s <= B; s += 32) {
             cu_blocks[s] = 0;
@@ -116,9 +115,9 @@ score_plan_kernel(const int32_t *__restrict__ cu, int32_t *__restrict__ cu_block
         cnt->blocks = (int32_t)base_b;
         cnt->rows = base_r;
         cnt->flagged = 0;
-        cnt->fin_done = 0;
         cnt->bar[0] = 0;
         cnt->bar[1] = 0;
+        cnt->bar[2] = 0;
     }
 }
 

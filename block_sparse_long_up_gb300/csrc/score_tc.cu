@@ -36,7 +36,9 @@
 // keys of the unit; the row's statistics for the chunk (ref and the sum of all
 // its block partials) go to workspace.  Later keys may exceed ref; fp32 absorbs
 // that up to ~115 binary orders of magnitude, and a tile whose sums overflow
-// anyway is queued for the exact CUDA-core fallback.
+// anyway is queued for an exact CUDA-core fallback in the epilogue.  After its
+// last unit every CTA runs the epilogue: grid barriers, then each row's
+// normaliser and chunk weights, then the block scores (see score_epilogue).
 #include <cudaTypedefs.h>
 
 #include "../../include/up.h"
@@ -49,7 +51,6 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 384;
 constexpr int kWarpTmaK = 0;
 constexpr int kWarpMma0 = 1;     // issues the MMAs of TMEM buffer 0
 constexpr int kWarpTmaQ = 2;
@@ -66,6 +67,11 @@ constexpr int kMaxStages = 16;
 
 template <int D>
 struct Cfg {
+    // Two softmax warpgroups (warpgroup e takes tile e of every pair).  Four
+    // (one tile each at head_dim <= 128) measured slower: only two TMEM buffers
+    // of two tiles fit, so the warpgroups of a buffer idle while it is refilled.
+    static constexpr int kWGs = 2;
+    static constexpr int kThreads = 128 * (1 + kWGs);
     static constexpr int kTiles = tiles_per_unit(D);
     static constexpr int kPairs = kTiles / 2;
     static constexpr int kPanels = D / 64;
@@ -93,7 +99,7 @@ struct Shared {
     uint32_t tmem_base;
     int units;
     int abort;
-    int epi_state;  // epilogue: 0 go on, 1 a wait expired, 2 tiles overflowed (the finish kernel redoes all)
+    int epi_state;  // epilogue: 0 go on, 1 a wait expired, 2 tiles were queued for the exact fallback
 };
 
 struct Unit {
@@ -682,12 +688,12 @@ __device__ __forceinline__ int find_seq_by_block(const SeqInfo *seqs, int B, int
 
 // Epilogue, all threads of every CTA, after the CTA's last unit:
 //   barrier 1 -- every unit of the grid is done: all partials and statistics
-//                are in memory (if a tile was queued for the exact fallback,
-//                stop here: the finish kernel redoes the rows and blocks);
-//   rows      -- a contiguous share of all softmax rows per CTA, one row per
-//                thread: over the row's key chunks c (in order, up to
-//                kEpiChunks of them loaded at once), the maximum M and
-//                normaliser l,
+//                are in memory; if tiles were queued for the exact fallback,
+//                the CTAs recompute them (fallback_tiles) and meet at one more
+//                barrier;
+//   rows      -- a contiguous share of all softmax rows per CTA, kRowLanes
+//                threads per row: over the row's key chunks c, the maximum M
+//                and normaliser l,
 //                  M = max_c mref[c][r],  l = sum_c lsum[c][r] * 2^(mref[c][r] - M),
 //                then, in place of mref[c][r], the weight of chunk c's
 //                partials, w = 2^(mref[c][r] - M) / (l * n_s * Hq_norm);
@@ -699,10 +705,9 @@ __device__ __forceinline__ int find_seq_by_block(const SeqInfo *seqs, int B, int
 //                order -- independent of the grid and the batching, so the
 //                scores are bitwise reproducible.
 // Loads of other CTAs' results bypass L1.
-constexpr int kEpiChunks = 24;  // chunk statistics a thread has in flight
+constexpr int kEpiChunks = 4;   // chunk statistics a thread has in flight (per kRowLanes chunks)
 constexpr int kEpiBlocks = 6;   // blocks of one batch (all of their partials in flight)
 constexpr int kEpiVec = 3;      // float4 groups per thread and block in flight (rows <= 4608)
-constexpr int kWarps = kThreads / 32;
 
 // Online merge of a row's (maximum, normaliser) with one chunk's (reference, sum).
 __device__ __forceinline__ void merge_chunk(float &M, float &l, float m, float s) {
@@ -717,63 +722,91 @@ __device__ __forceinline__ void merge_chunk(float &M, float &l, float m, float s
     M = mn;
 }
 
+// Rows: kRowLanes consecutive threads take one row, each the chunks c = sub,
+// sub + kRowLanes, ... (at most kEpiChunks per thread loaded at once); their
+// (maximum, normaliser) pairs are merged by a fixed butterfly, so every lane
+// ends with the row's M and l (bitwise the same whichever CTA does the row).
+constexpr int kRowLanes = 8;
+
+template <int NT>
 __device__ void epilogue_rows(const ScoreParams &p) {
     const int64_t total = p.counters->rows;
     const int64_t per = (total + gridDim.x - 1) / gridDim.x;
     const int64_t r0 = (int64_t)blockIdx.x * per, r1 = min(r0 + per, total);
-    for (int64_t gr = r0 + threadIdx.x; gr < r1; gr += kThreads) {
-        const SeqInfo &sq = p.num_seqs == 1 ? p.seq0 : p.seqs[find_seq_by_row(p.seqs, p.num_seqs, gr)];
-        const int64_t r = gr - sq.row_off;
+    const int sub = threadIdx.x % kRowLanes;
+    constexpr int kRowsPerPass = NT / kRowLanes;
+    for (int64_t g0 = r0; g0 < r1; g0 += kRowsPerPass) {
+        const int64_t gr = g0 + threadIdx.x / kRowLanes;
+        const bool row_ok = gr < r1;
+        const SeqInfo &sq = p.num_seqs == 1
+                                ? p.seq0
+                                : p.seqs[find_seq_by_row(p.seqs, p.num_seqs, row_ok ? gr : r0)];
+        const int64_t r = (row_ok ? gr : r0) - sq.row_off;
         float *mref = p.mref + sq.stat_off + r;
         const float *lsum = p.lsum + sq.stat_off + r;
-        const float norm = (float)sq.ns * (float)p.Hq_norm;
+        const int nch = row_ok ? sq.nchunks : 0;
         float M = -INFINITY, l = 0.f;
-        if (sq.nchunks <= kEpiChunks) {
-            // every chunk's statistics in flight at once, kept for the weights
+        // this lane's chunks c = sub + kRowLanes * k; the first kEpiChunks of
+        // them stay in registers for the weights
+        float m0[kEpiChunks];
+#pragma unroll
+        for (int k = 0; k < kEpiChunks; ++k) {
+            const int c = sub + k * kRowLanes;
+            m0[k] = c < nch ? __ldcg(mref + (int64_t)c * sq.R) : -INFINITY;
+        }
+        {
+            float s[kEpiChunks];
+#pragma unroll
+            for (int k = 0; k < kEpiChunks; ++k) {
+                const int c = sub + k * kRowLanes;
+                s[k] = c < nch ? __ldcg(lsum + (int64_t)c * sq.R) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < kEpiChunks; ++k) merge_chunk(M, l, m0[k], s[k]);
+        }
+        for (int c0 = sub + kRowLanes * kEpiChunks; c0 < nch; c0 += kRowLanes * kEpiChunks) {
             float m[kEpiChunks], s[kEpiChunks];
 #pragma unroll
             for (int k = 0; k < kEpiChunks; ++k) {
-                const bool ok = k < sq.nchunks;
-                m[k] = ok ? __ldcg(mref + (int64_t)k * sq.R) : -INFINITY;
-                s[k] = ok ? __ldcg(lsum + (int64_t)k * sq.R) : 0.f;
-            }
-#pragma unroll
-            for (int k = 0; k < kEpiChunks; ++k) merge_chunk(M, l, m[k], s[k]);
-            const float inv = (M == -INFINITY || !(l > 0.f)) ? 0.f : 1.0f / (l * norm);
-#pragma unroll
-            for (int k = 0; k < kEpiChunks; ++k)
-                if (k < sq.nchunks)
-                    mref[(int64_t)k * sq.R] =
-                        (m[k] == -INFINITY || inv == 0.f) ? 0.f : exp2f(m[k] - M) * inv;
-            continue;
-        }
-        for (int c0 = 0; c0 < sq.nchunks; c0 += kEpiChunks) {
-            float m[kEpiChunks], s[kEpiChunks];
-#pragma unroll
-            for (int k = 0; k < kEpiChunks; ++k) {
-                const bool ok = c0 + k < sq.nchunks;
-                m[k] = ok ? __ldcg(mref + (int64_t)(c0 + k) * sq.R) : -INFINITY;
-                s[k] = ok ? __ldcg(lsum + (int64_t)(c0 + k) * sq.R) : 0.f;
+                const int c = c0 + k * kRowLanes;
+                m[k] = c < nch ? __ldcg(mref + (int64_t)c * sq.R) : -INFINITY;
+                s[k] = c < nch ? __ldcg(lsum + (int64_t)c * sq.R) : 0.f;
             }
 #pragma unroll
             for (int k = 0; k < kEpiChunks; ++k) merge_chunk(M, l, m[k], s[k]);
         }
-        const float inv = (M == -INFINITY || !(l > 0.f)) ? 0.f : 1.0f / (l * norm);
-        for (int c0 = 0; c0 < sq.nchunks; c0 += kEpiChunks) {
-            float m[kEpiChunks];
 #pragma unroll
-            for (int k = 0; k < kEpiChunks; ++k)
-                m[k] = c0 + k < sq.nchunks ? __ldcg(mref + (int64_t)(c0 + k) * sq.R) : -INFINITY;
+        for (int o = 1; o < kRowLanes; o <<= 1) {
+            const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+            const float lo = __shfl_xor_sync(0xffffffffu, l, o);
+            // the lower lane's pair first, so both lanes compute the same bits
+            if ((sub & o) == 0) merge_chunk(M, l, Mo, lo);
+            else {
+                float M2 = Mo, l2 = lo;
+                merge_chunk(M2, l2, M, l);
+                M = M2;
+                l = l2;
+            }
+        }
+        const float inv = (M == -INFINITY || !(l > 0.f))
+                              ? 0.f
+                              : 1.0f / (l * (float)sq.ns * (float)p.Hq_norm);
+        auto weight = [&](float m) { return (m == -INFINITY || inv == 0.f) ? 0.f : exp2f(m - M) * inv; };
 #pragma unroll
-            for (int k = 0; k < kEpiChunks; ++k)
-                if (c0 + k < sq.nchunks)
-                    mref[(int64_t)(c0 + k) * sq.R] =
-                        (m[k] == -INFINITY || inv == 0.f) ? 0.f : exp2f(m[k] - M) * inv;
+        for (int k = 0; k < kEpiChunks; ++k) {
+            const int c = sub + k * kRowLanes;
+            if (c < nch) mref[(int64_t)c * sq.R] = weight(m0[k]);
+        }
+        for (int c = sub + kRowLanes * kEpiChunks; c < nch; c += kRowLanes) {
+            float *q = mref + (int64_t)c * sq.R;
+            *q = weight(__ldcg(q));
         }
     }
 }
 
-__device__ void epilogue_blocks(const ScoreParams &p, float (*red)[kWarps]) {
+template <int NT>
+__device__ void epilogue_blocks(const ScoreParams &p, float (*red)[NT / 32]) {
+    constexpr int kWarps = NT / 32;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int nbt = p.counters->blocks;
     const int per = (nbt + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -797,18 +830,18 @@ __device__ void epilogue_blocks(const ScoreParams &p, float (*red)[kWarps]) {
             const float4 *p4 = reinterpret_cast<const float4 *>(pt);
             const int R4 = sq.R / 4;
             const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int i0 = threadIdx.x; i0 < R4; i0 += kEpiVec * kThreads) {
+            for (int i0 = threadIdx.x; i0 < R4; i0 += kEpiVec * NT) {
                 float4 w[kEpiVec], x[kEpiBlocks][kEpiVec];
 #pragma unroll
                 for (int u = 0; u < kEpiVec; ++u) {
-                    const int i = i0 + u * kThreads;
+                    const int i = i0 + u * NT;
                     w[u] = i < R4 ? __ldcg(w4 + i) : zero;
                 }
 #pragma unroll
                 for (int k = 0; k < kEpiBlocks; ++k)
 #pragma unroll
                     for (int u = 0; u < kEpiVec; ++u) {
-                        const int i = i0 + u * kThreads;
+                        const int i = i0 + u * NT;
                         x[k][u] = (k < nbat && i < R4) ? __ldcg(p4 + (int64_t)k * R4 + i) : zero;
                     }
 #pragma unroll
@@ -817,7 +850,7 @@ __device__ void epilogue_blocks(const ScoreParams &p, float (*red)[kWarps]) {
                     for (int u = 0; u < kEpiVec; ++u) acc[k] = dot4(x[k][u], w[u], acc[k]);
             }
         } else {
-            for (int r = threadIdx.x; r < sq.R; r += kThreads) {
+            for (int r = threadIdx.x; r < sq.R; r += NT) {
                 const float w = __ldcg(wr + r);
 #pragma unroll
                 for (int k = 0; k < kEpiBlocks; ++k)
@@ -845,18 +878,136 @@ __device__ void epilogue_blocks(const ScoreParams &p, float (*red)[kWarps]) {
     }
 }
 
+// The exact fallback for the rare row tiles whose fp32 sums overflowed in the
+// main loop: a logit more than ~115 binary orders of magnitude above the
+// unit's reference (taken from its first 32 keys).  Each queued tile (4 *
+// unit + tile) is recomputed by one CTA on the CUDA cores with two passes over
+// the unit's keys: the first finds each row's exact maximum m (log2 units),
+// the second sums 2^(z*log2e/sqrt(d) - m) over every block; the tile's
+// partials and chunk statistics are rewritten.  Row r of the tile is thread r
+// (128 of the CTA's threads compute; all of them stage Q and K in shared
+// memory).  The queue is empty for ordinary attention logits.
+constexpr int kKeyTile = 32;
+
+template <int D>
+__device__ __forceinline__ void tile_logits(const __nv_bfloat16 *qT, const float *ks, int tid,
+                                            float (&acc)[kKeyTile]) {
+#pragma unroll
+    for (int kk = 0; kk < kKeyTile; ++kk) acc[kk] = 0.f;
+    for (int c = 0; c < D; ++c) {
+        const float qv = __bfloat162float(qT[c * kRowsPerTile + tid]);
+#pragma unroll
+        for (int kk = 0; kk < kKeyTile; ++kk) acc[kk] = fmaf(qv, ks[kk * D + c], acc[kk]);
+    }
+}
+
+template <int D>
+__device__ void fallback_tiles(const ScoreParams &p, unsigned char *smem) {
+    const int nflag =
+        min(*reinterpret_cast<const volatile int32_t *>(&p.counters->flagged), p.flag_cap);
+    __nv_bfloat16 *qT = reinterpret_cast<__nv_bfloat16 *>(smem);         // [D][128]
+    float *ks = reinterpret_cast<float *>(smem + D * kRowsPerTile * 2);  // [32][D]
+    const int tid = threadIdx.x;
+    const bool row_thread = tid < kRowsPerTile;
+    for (int fi = blockIdx.x; fi < nflag; fi += gridDim.x) {
+        const int entry = __ldcg(p.flag_list + fi);
+        const int u = entry >> 2;  // work unit; low two bits: which of its row tiles
+        const int s = find_seq_by_unit(p.seqs, p.num_seqs, u);
+        const SeqInfo sq = p.seqs[s];
+        int loc = u - sq.unit_off;
+        const int mt = (loc % sq.mtiles) * tiles_per_unit(D) + (entry & 3);
+        loc /= sq.mtiles;
+        const int c = loc % sq.nchunks;
+        const int j = loc / sq.nchunks;
+        const int grows = p.g * sq.ns;
+        // row tid of the tile: query t = mt * tpt + tid / g of query head j * g + h
+        const int tl = tid / p.g, h = tid - tl * p.g;
+        const int t = mt * p.tpt + tl;
+        const bool valid = row_thread && tid < p.g * p.tpt && t < sq.ns;
+        const int a = sq.L - sq.ns + (valid ? t : 0);
+        const int64_t r = (int64_t)j * grows + (int64_t)t * p.g + h;
+        __syncthreads();
+        for (int idx = tid; idx < kRowsPerTile * D; idx += Cfg<D>::kThreads) {
+            const int row = idx / D, cc = idx % D;
+            const int rtl = row / p.g, rh = row - rtl * p.g, rt = mt * p.tpt + rtl;
+            __nv_bfloat16 v = __float2bfloat16(0.f);
+            if (row < p.g * p.tpt && rt < sq.ns)
+                v = p.q[((int64_t)(sq.q_off + rt) * p.Hq + j * p.g + rh) * D + cc];
+            qT[cc * kRowsPerTile + row] = v;
+        }
+        const int k0 = c * p.C;
+        const int k1 = min(k0 + p.C, sq.L);
+        float m = -INFINITY, lsum = 0.f;
+        float acc[kKeyTile];
+        for (int pass = 0; pass < 2; ++pass) {
+            float bsum = 0.f;
+            for (int kt = k0; kt < k1; kt += kKeyTile) {
+                __syncthreads();
+                for (int idx = tid; idx < kKeyTile * D; idx += Cfg<D>::kThreads) {
+                    const int key = kt + idx / D;
+                    float v = 0.f;
+                    if (key < k1) {
+                        if (!p.block_table) {
+                            v = __bfloat162float(
+                                p.k[((int64_t)(sq.tok_off + key) * p.Hk + j) * D + idx % D]);
+                        } else {
+                            const int64_t row = paged_row(p, s, j, key);
+                            if (row < p.num_pages * p.Hk * p.page_size)
+                                v = __bfloat162float(p.k[row * D + idx % D]);
+                        }
+                    }
+                    ks[idx] = v;
+                }
+                __syncthreads();
+                if (!row_thread) continue;
+                tile_logits<D>(qT, ks, tid, acc);
+#pragma unroll
+                for (int kk = 0; kk < kKeyTile; ++kk) {
+                    const int key = kt + kk;
+                    if (key >= k1) break;
+                    const bool vis = key <= a;
+                    const float z = acc[kk] * p.scale_log2;
+                    if (pass == 0) {
+                        if (vis) m = fmaxf(m, z);
+                    } else {
+                        const float e = (vis && m != -INFINITY) ? exp2f(z - m) : 0.f;
+                        bsum += e;
+                        if ((key + 1) % p.G == 0 || key + 1 == k1) {
+                            if (valid) p.part[sq.part_off + (int64_t)(key / p.G) * sq.R + r] = bsum;
+                            lsum += bsum;
+                            bsum = 0.f;
+                        }
+                    }
+                }
+            }
+        }
+        if (valid) {
+            const int64_t o = sq.stat_off + (int64_t)(kSlotsPerChunk * c) * sq.R + r;
+            p.mref[o] = m;
+            p.lsum[o] = lsum;
+        }
+    }
+}
+
 template <int D>
 __device__ void score_epilogue(const ScoreParams &p, Shared &sh, float *smem_f) {
     pdl_wait();  // the plan's table and counters
     Counters *cnt = const_cast<Counters *>(p.counters);
-    if (grid_barrier(p, &cnt->bar[0], sh, true) != 0) return;
-    epilogue_rows(p);
+    const int st = grid_barrier(p, &cnt->bar[0], sh, true);
+    if (st == 1) return;  // a wait expired
+    if (st == 2) {
+        // tiles overflowed: recompute them exactly before the rows read them
+        fallback_tiles<D>(p, reinterpret_cast<unsigned char *>(smem_f));
+        if (grid_barrier(p, &cnt->bar[2], sh, false) != 0) return;
+    }
+    epilogue_rows<Cfg<D>::kThreads>(p);
     if (grid_barrier(p, &cnt->bar[1], sh, false) != 0) return;
-    epilogue_blocks(p, reinterpret_cast<float(*)[kWarps]>(smem_f));
+    epilogue_blocks<Cfg<D>::kThreads>(
+        p, reinterpret_cast<float(*)[Cfg<D>::kThreads / 32]>(smem_f));
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                 const ScoreParams p) {
     using C = Cfg<D>;
@@ -997,7 +1148,8 @@ cudaError_t launch_dg(const ScoreParams &p, const ScoreLayout &lay, int num_sms,
     if (e != cudaSuccess) return e;
     const int64_t grid = lay.max_units < num_sms ? lay.max_units : num_sms;
     if (grid < 1) return cudaSuccess;
-    return launch_pdl(score_tc_kernel<D, G>, dim3((unsigned)grid), dim3(kThreads), Cfg<D>::kSmem, st,
+    return launch_pdl(score_tc_kernel<D, G>, dim3((unsigned)grid), dim3(Cfg<D>::kThreads),
+                      Cfg<D>::kSmem, st,
                       km, qm, p);
 }
 

@@ -425,10 +425,10 @@ def test_overflowing_unit_takes_the_exact_fallback():
     torch.cuda.synchronize()
     flagged = int(ws[256 + 16:256 + 20].view(torch.int32).item())
     assert flagged > 0, "the overflowing unit was not queued for the fallback"
-    # with a queue, the CTAs of the finishing kernel count themselves done and
-    # the last one computes the row statistics
-    fin_done = int(ws[256 + 20:256 + 24].view(torch.int32).item())
-    assert fin_done > 0
+    # with a queue, every CTA of the scoring kernel recomputes its share of the
+    # queued tiles and then arrives at the fallback's grid barrier
+    fallback_barrier = int(ws[256 + 28:256 + 32].view(torch.int32).item())
+    assert fallback_barrier > 0
     orc_sc, orc_cb = oracle.score_blocks(inp.q_last, inp.k, inp.cu_seqlens, 32, 8, 128, 128, 64)
     g_sc = sc[: int(orc_cb[-1])].cpu().numpy().astype(np.float64)
     nbad, worst = score_failures(g_sc, orc_sc)
