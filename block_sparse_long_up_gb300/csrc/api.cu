@@ -408,6 +408,7 @@ up_status up_compact(const void *x, const int32_t *pos, int hidden, const int32_
     a.dst_blk = reinterpret_cast<int32_t *>(ws + lay.dst_blk);
     a.err = ds->err;
     a.max_blocks = total_tokens / G + num_seqs;
+    a.nb_one = num_seqs == 1 ? (int)((total_tokens + G - 1) / G) : -1;
     a.num_seqs = num_seqs;
     a.G = G;
     a.hidden = hidden;

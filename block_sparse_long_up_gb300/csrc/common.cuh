@@ -185,6 +185,7 @@ struct CompactArgs {
     int32_t *dst_blk;  // scratch: destination row of every block
     unsigned int *err; // the device error word
     int64_t max_blocks;  // total_tokens / G + num_seqs: the most blocks the batch can have
+    int nb_one;          // one sequence: ceil(total_tokens / G), its block count; else -1
     int num_seqs, G, hidden, rows_per_item, items_per_block;
     int64_t vec_per_row;  // hidden * 2 / 16
 };

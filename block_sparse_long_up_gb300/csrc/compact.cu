@@ -109,7 +109,10 @@ compact_one_kernel(CompactArgs a) {
     __shared__ int npiece;
     pdl_wait();
     const int B = a.num_seqs, t = threadIdx.x;
-    const int nbt = a.cu_blocks[B];
+    // one sequence: the block count is the host's (the flags' loads need not
+    // wait for cu_blocks); cu_blocks[1] is still checked against it, below
+    const bool one = a.nb_one >= 0;
+    const int nbt = one ? a.nb_one : a.cu_blocks[B];
     if (!block_count_ok(a, nbt)) {
         if (blockIdx.x == 0 && t == 0) {
             atomicOr(a.err, UP_DEVERR_BAD_CU_BLOCKS);
@@ -117,13 +120,16 @@ compact_one_kernel(CompactArgs a) {
         }
         return;
     }
+    const int L0 = one ? a.cu_seqlens[1] - a.cu_seqlens[0] : 0;
     const int per = (nbt + kOneThreads - 1) / kOneThreads;
     const int g0 = min(t * per, nbt), g1 = min(g0 + per, nbt);
-    const int s0 = g0 < g1 ? seq_of_block(a.cu_blocks, B, g0) : 0;
+    const int s0 = g0 < g1 && !one ? seq_of_block(a.cu_blocks, B, g0) : 0;
+    auto rows_of = [&](int s, int gb) { return one ? min(a.G, L0 - gb * a.G) : block_rows(a, s, gb); };
     int rows = 0;
     for (int gb = g0, s = s0; gb < g1; ++gb) {
-        while (a.cu_blocks[s + 1] <= gb) ++s;
-        if (a.keep[gb]) rows += block_rows(a, s, gb);
+        if (!one)
+            while (a.cu_blocks[s + 1] <= gb) ++s;
+        if (a.keep[gb]) rows += rows_of(s, gb);
     }
     int64_t T64;
     const int first = (int)block_excl_scan_i64(rows, &T64, scan_sh);
@@ -137,12 +143,15 @@ compact_one_kernel(CompactArgs a) {
     if (first < hi && first + rows > lo) {
         int dst = first;
         for (int gb = g0, s = s0; gb < g1 && dst < hi; ++gb) {
-            while (a.cu_blocks[s + 1] <= gb) ++s;
+            if (!one)
+                while (a.cu_blocks[s + 1] <= gb) ++s;
             if (!a.keep[gb]) continue;
-            const int len = block_rows(a, s, gb);
+            const int len = rows_of(s, gb);
             if (dst + len > lo) {
                 const int c0 = max(dst, lo), c1 = min(dst + len, hi);
-                const int src = a.cu_seqlens[s] + (gb - a.cu_blocks[s]) * a.G + (c0 - dst);
+                const int src = (one ? a.cu_seqlens[0] + gb * a.G
+                                     : a.cu_seqlens[s] + (gb - a.cu_blocks[s]) * a.G) +
+                                (c0 - dst);
                 const int i = atomicAdd(&npiece, 1);
                 if (i < kOnePieces) piece[i] = make_int4(src, c0, c1 - c0, 0);
             }
@@ -161,6 +170,9 @@ compact_one_kernel(CompactArgs a) {
         }
     }
     if (blockIdx.x == 0) {
+        // one sequence: cu_blocks must be {0, nbt} (the batch's own)
+        const bool bad = one && (a.cu_blocks[0] != 0 || a.cu_blocks[1] != nbt);
+        if (bad && t == 0) atomicOr(a.err, UP_DEVERR_BAD_CU_BLOCKS);
         // cu_seqlens_out[s]: the output row of sequence s's first block -- the
         // first row of the range holding it plus the kept rows before it there
         for (int s = t; s <= B; s += kOneThreads) {
@@ -174,7 +186,7 @@ compact_one_kernel(CompactArgs a) {
             }
             a.cu_out[s] = v;
         }
-        if (t == 0) *a.total_kept = T;
+        if (t == 0) *a.total_kept = bad ? 0 : T;
     }
 }
 

@@ -263,10 +263,11 @@ up_status up_select_blocks(const float *scores, const int32_t *cu_blocks,
  *   total_kept      int32 [1] (output): number of kept rows (= cu_seqlens_out[num_seqs]).
  *   workspace       at least up_compact_workspace(...) bytes, 256-byte aligned.
  * The output size lives on the device; reading it on the host is the caller's
- * choice (one device-to-host copy of total_kept).  A cu_blocks whose last entry
- * is negative or above total_tokens/G + num_seqs (not one that up_score_blocks
- * wrote for this batch) sets UP_DEVERR_BAD_CU_BLOCKS; nothing is copied and
- * total_kept is 0.
+ * choice (one device-to-host copy of total_kept).  A cu_blocks that cannot be
+ * this batch's (its last entry negative or above total_tokens/G + num_seqs;
+ * for one sequence, anything but {0, ceil(total_tokens/G)}) sets
+ * UP_DEVERR_BAD_CU_BLOCKS and total_kept is 0; nothing is read or written out
+ * of bounds, and the other outputs are unspecified.
  */
 size_t up_compact_workspace(int num_seqs, int64_t total_tokens, int G);
 
