@@ -655,6 +655,17 @@ def run_ours(args, inp, w, rank, world):
     E = args.e2e_steps
     h_total = torch.empty(1, dtype=torch.int32).pin_memory()
     h_cuo = torch.empty(inp.num_seqs + 1, dtype=torch.int32).pin_memory()
+    # the copies' own bandwidth (events around each, one pass before the loop)
+    cev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    torch.cuda.synchronize()
+    cev[0].record(stream)
+    k.copy_(h_k, non_blocking=True)
+    cev[1].record(stream)
+    x.copy_(h_x, non_blocking=True)
+    cev[2].record(stream)
+    torch.cuda.synchronize()
+    h2d_gbs = dict(k=h_k.nbytes / (cev[0].elapsed_time(cev[1]) * 1e-3) / 1e9,
+                   x=h_x.nbytes / (cev[1].elapsed_time(cev[2]) * 1e-3) / 1e9)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -689,7 +700,9 @@ def run_ours(args, inp, w, rank, world):
         config=workload_config(args, inp, w, world),
         clocks=clk,
         e2e=(dict(value=world * inp.total_tokens / e2e_s, unit=UNIT, h2d_bytes_per_step=h2d,
-                  d2h_bytes_per_step=d2h, ms_per_step=e2e_s * 1e3) if e2e_s else None),
+                  d2h_bytes_per_step=d2h, ms_per_step=e2e_s * 1e3,
+                  h2d_copy_gbs={n: round(v, 1) for n, v in h2d_gbs.items()})
+             if e2e_s else None),
         gpu_launches=K * sp.launches_per_step(),
         roofline=dict(kernel="score_tc_kernel (tcgen05 scoring)", bound="tensor",
                       achieved=achieved, peak=tc_burst, unit="TFLOP/s", frac=achieved / tc_burst,

@@ -106,13 +106,13 @@ __device__ __forceinline__ unsigned long long block_scan_u64(unsigned long long 
     if (lane == 31) sh.wsum[wid] = x;
     __syncthreads();
     if (wid == 0) {
-        unsigned long long w = sh.wsum[lane];
+        unsigned long long w = lane < kSelWarps ? sh.wsum[lane] : 0ull;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
-        sh.wsum[lane] = w;
+        if (lane < kSelWarps) sh.wsum[lane] = w;
     }
     __syncthreads();
     *total = sh.wsum[kSelWarps - 1];
@@ -266,7 +266,7 @@ __device__ void select_seq(const float *__restrict__ scores, int b0, int nb, int
     if (lane == 0) sh.kept[wid] = kept;
     __syncthreads();
     if (t < 32) {
-        int w = sh.kept[t];
+        int w = t < kSelWarps ? sh.kept[t] : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
         if (t == 0) kept_tokens[s] = w;
