@@ -242,15 +242,21 @@ done:
 // a stage is refilled only after both have released it.  head_dim 256 (one
 // pair): buffer = parity of the CTA-wide K step count, and each stage is used
 // and released by that step's issuer alone.
+// The whole warp walks the loop, so the control flow and the descriptors are
+// warp-uniform, and one elected lane issues the MMAs and commits: a lone
+// thread's instructions, competing with two softmax warps on its SM
+// sub-partition, issued one M128 x N128 MMA every ~107 cycles (64 at full rate).
 template <int D>
 __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_t *kbuf,
                          uint32_t tmem, int units, int w) {
     using C = Cfg<D>;
     constexpr uint32_t idesc = idesc_bf16_f32(kRowsPerTile, kStepKeys);
     volatile int *abort = &sh.abort;
+    const bool leader = elect_one();
     uint32_t it = 0, gstep = 0, tuse = 0;  // K panels, K steps, uses of TMEM buffer w
     uint32_t qpar = 0u;  // bit qs: parity of the Q loads into pair buffer qs so far
     const uint32_t d_base = tmem + (uint32_t)(w * kBufCols);
+    const uint32_t kbase = smem_u32(kbuf), qbase = smem_u32(qbuf);
     uint32_t ui = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++ui) {
         Unit un;
@@ -271,33 +277,39 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
                 // after its MMAs, so a stage is held ~0.3 us instead of a step.
                 if ((gstep & 1u) != (uint32_t)w) continue;  // the other issuer's step
                 if (!q_ready) {
-                    if (!mbar_wait(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort, p.wait_limit))
+                    if (!mbar_wait_warp(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort,
+                                        p.wait_limit))
                         goto out;
                     q_ready = true;
                 }
-                if (!mbar_wait(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, p.wait_limit))
+                if (!mbar_wait_warp(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, p.wait_limit))
                     goto out;
                 tc_fence_after();
 #pragma unroll 1
                 for (int pn = 0; pn < C::kPanels; ++pn) {
                     const uint32_t i = it0 + pn;
-                    const int st = i % C::kStages;
-                    if (!mbar_wait(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort, p.wait_limit))
+                    const uint32_t st = i % C::kStages;
+                    if (!mbar_wait_warp(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort,
+                                        p.wait_limit))
                         goto out;
                     tc_fence_after();
-                    const uint64_t bd = smem_desc_sw128(smem_u32(kbuf + st * kPanelBytesK));
+                    const uint64_t bd = smem_desc_sw128(kbase + st * kPanelBytesK);
+                    if (leader) {
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const uint64_t ad = smem_desc_sw128(smem_u32(
-                            qbuf + qs * C::kQPairBytes + e * C::kQTileBytes + pn * kPanelBytesQ));
+                        for (int e = 0; e < 2; ++e) {
+                            const uint64_t ad = smem_desc_sw128(
+                                qbase + qs * C::kQPairBytes + e * C::kQTileBytes + pn * kPanelBytesQ);
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)  // 4 x K=16 per 64-wide panel (32 B)
-                            mma_bf16(d_base + (uint32_t)(e * kStepKeys), ad + 2 * ks, bd + 2 * ks,
-                                     idesc, (pn | ks) != 0);
+                            for (int ks = 0; ks < 4; ++ks)  // 4 x K=16 per 64-wide panel (32 B)
+                                mma_bf16(d_base + (uint32_t)(e * kStepKeys), ad + 2 * ks,
+                                         bd + 2 * ks, idesc, (pn | ks) != 0);
+                        }
+                        mma_commit(smem_u32(&sh.kempty[st]));
                     }
-                    mma_commit(smem_u32(&sh.kempty[st]));
+                    __syncwarp();
                 }
-                mma_commit(smem_u32(&sh.tfull[w]));
+                if (leader) mma_commit(smem_u32(&sh.tfull[w]));
+                __syncwarp();
                 ++tuse;
             } else {
                 // head_dim <= 128: pair w uses buffer w, and both issuers walk
@@ -311,49 +323,58 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
                 // as soon as the buffer is free.
                 for (int pn = 0; pn < C::kPanels; ++pn) {
                     const uint32_t i = it0 + pn;
-                    if (!mbar_wait(smem_u32(&sh.kfull[i % C::kStages]), (i / C::kStages) & 1,
-                                   abort, p.wait_limit))
+                    if (!mbar_wait_warp(smem_u32(&sh.kfull[i % C::kStages]), (i / C::kStages) & 1,
+                                        abort, p.wait_limit))
                         goto out;
                 }
                 if (pair_ok) {
                     if (!q_ready) {
-                        if (!mbar_wait(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort,
-                                       p.wait_limit))
+                        if (!mbar_wait_warp(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort,
+                                            p.wait_limit))
                             goto out;
                         q_ready = true;
                     }
-                    if (!mbar_wait(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, p.wait_limit))
+                    if (!mbar_wait_warp(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort,
+                                        p.wait_limit))
                         goto out;
                     tc_fence_after();
+                    if (leader) {
 #pragma unroll
-                    for (int pn = 0; pn < C::kPanels; ++pn) {
-                        const int st = (it0 + pn) % C::kStages;
-                        const uint64_t bd = smem_desc_sw128(smem_u32(kbuf + st * kPanelBytesK));
+                        for (int pn = 0; pn < C::kPanels; ++pn) {
+                            const uint32_t st = (it0 + pn) % C::kStages;
+                            const uint64_t bd = smem_desc_sw128(kbase + st * kPanelBytesK);
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const uint64_t ad = smem_desc_sw128(
-                                smem_u32(qbuf + qs * C::kQPairBytes + e * C::kQTileBytes +
-                                         pn * kPanelBytesQ));
+                            for (int e = 0; e < 2; ++e) {
+                                const uint64_t ad = smem_desc_sw128(qbase + qs * C::kQPairBytes +
+                                                                    e * C::kQTileBytes +
+                                                                    pn * kPanelBytesQ);
 #pragma unroll
-                            for (int ks = 0; ks < 4; ++ks)  // 4 x K=16 per 64-wide panel (32 B)
-                                mma_bf16(d_base + (uint32_t)(e * kStepKeys), ad + 2 * ks,
-                                         bd + 2 * ks, idesc, (pn | ks) != 0);
+                                for (int ks = 0; ks < 4; ++ks)  // 4 x K=16 per 64-wide panel
+                                    mma_bf16(d_base + (uint32_t)(e * kStepKeys), ad + 2 * ks,
+                                             bd + 2 * ks, idesc, (pn | ks) != 0);
+                            }
                         }
+                        mma_commit(smem_u32(&sh.tfull[w]));
                     }
-                    mma_commit(smem_u32(&sh.tfull[w]));
+                    __syncwarp();
                 }
-                for (int pn = 0; pn < C::kPanels; ++pn)
-                    mma_commit(smem_u32(&sh.kempty[(it0 + pn) % C::kStages]));
+                if (leader) {
+                    for (int pn = 0; pn < C::kPanels; ++pn)
+                        mma_commit(smem_u32(&sh.kempty[(it0 + pn) % C::kStages]));
+                }
+                __syncwarp();
                 if (pair_ok) ++tuse;
             }
         }
         // the pair buffer is free once this issuer's MMAs on it have completed
-        if (C::kPairs == 1 || pair_ok) mma_commit(smem_u32(&sh.qempty[qs]));
+        if ((C::kPairs == 1 || pair_ok) && leader) mma_commit(smem_u32(&sh.qempty[qs]));
+        __syncwarp();
         for (int pr = 0; pr < un.npairs; ++pr) qpar ^= 1u << (qb + pr);
     }
 out:
-    // every MMA issued by this thread has completed once fin fires
-    mma_commit(smem_u32(&sh.fin[w]));
+    // every MMA issued by this warp has completed once fin fires
+    if (leader) mma_commit(smem_u32(&sh.fin[w]));
+    __syncwarp();
     mbar_drain(smem_u32(&sh.fin[w]), 0);
 }
 
@@ -1067,7 +1088,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     } else if (warp == kWarpTmaQ) {
         if (lane == 0) role_tma_q<D>(&qmap, p, sh, qbuf, units);
     } else if (warp == kWarpMma0 || warp == kWarpMma1) {
-        if (lane == 0) role_mma<D>(p, sh, qbuf, kbuf, tmem, units, warp == kWarpMma0 ? 0 : 1);
+        role_mma<D>(p, sh, qbuf, kbuf, tmem, units, warp == kWarpMma0 ? 0 : 1);
     } else {
         role_softmax<D, G>(p, sh, tmem, units);
     }

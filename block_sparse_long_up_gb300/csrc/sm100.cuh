@@ -76,6 +76,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// One lane of a converged warp: true in exactly one lane (elect.sync), so a
+// single-thread operation (an MMA, a commit) can sit in warp-uniform code.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// mbar_wait for a whole warp: every lane polls, and the result is the same in
+// every lane (false if any lane saw the abort or the limit).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort,
+                                               long long limit) {
+    const bool ok = mbar_wait(bar, parity, abort, limit);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
