@@ -652,24 +652,43 @@ def run_ours(args, inp, w, rank, world):
         calls.update(extra_calls(up, sp, q, k, cu, inp, n, G, KB))
 
     # end to end: host (pinned) inputs -> device, the three calls, result -> host
+    # Every step's inputs come from pinned host memory: q, k and cu_seqlens are
+    # copied to the device; x and pos are read in place by the compaction,
+    # which takes only the kept rows across the host link (up_compact accepts
+    # pinned host rows); the kept count and cu_seqlens_out are read back.
     E = args.e2e_steps
     h_total = torch.empty(1, dtype=torch.int32).pin_memory()
     h_cuo = torch.empty(inp.num_seqs + 1, dtype=torch.int32).pin_memory()
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(E):
-        q.copy_(h_q, non_blocking=True)
-        k.copy_(h_k, non_blocking=True)
-        x.copy_(h_x, non_blocking=True)
-        cu.copy_(h_cu, non_blocking=True)
-        pos.copy_(h_pos, non_blocking=True)
-        sp.run(q, k, cu, x, pos)
-        h_total.copy_(sp.total_kept, non_blocking=True)
-        h_cuo.copy_(sp.cu_out, non_blocking=True)
+
+    def e2e_loop(steps, copy_rows):
+        # one untimed step first: the first pass over the pinned buffers pays
+        # one-off costs (35-120 ms in one run of this bench, 3 ms in isolation)
+        if steps <= 0:
+            return None
+        barrier(world)
         torch.cuda.synchronize()
-        assert int(h_total[0]) == kept
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / E, world) if E > 0 else None
+        t0 = None
+        for i in range(steps + 1):
+            if i == 1:
+                t0 = time.perf_counter()
+            q.copy_(h_q, non_blocking=True)
+            k.copy_(h_k, non_blocking=True)
+            cu.copy_(h_cu, non_blocking=True)
+            if copy_rows:
+                x.copy_(h_x, non_blocking=True)
+                pos.copy_(h_pos, non_blocking=True)
+                sp.run(q, k, cu, x, pos)
+            else:
+                sp.run(q, k, cu, h_x, h_pos)
+            h_total.copy_(sp.total_kept, non_blocking=True)
+            h_cuo.copy_(sp.cu_out, non_blocking=True)
+            torch.cuda.synchronize()
+            assert int(h_total[0]) == kept
+        return max_over_ranks((time.perf_counter() - t0) / steps, world)
+
+    e2e_s = e2e_loop(E, copy_rows=False)
+    # diagnostic: the same steps with x and pos copied to the device whole first
+    e2e_copy_s = e2e_loop(min(E, 3), copy_rows=True)
     # the copies' own bandwidth (events around each, one pass after the loop, on
     # the pinned buffers the timed steps have already used)
     cev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
@@ -682,7 +701,9 @@ def run_ours(args, inp, w, rank, world):
     torch.cuda.synchronize()
     h2d_gbs = dict(k=h_k.nbytes / (cev[0].elapsed_time(cev[1]) * 1e-3) / 1e9,
                    x=h_x.nbytes / (cev[1].elapsed_time(cev[2]) * 1e-3) / 1e9)
-    h2d = h_q.nbytes + h_k.nbytes + h_x.nbytes + h_cu.nbytes + h_pos.nbytes
+    h2d_copied = h_q.nbytes + h_k.nbytes + h_cu.nbytes
+    h2d_in_place = kept * (h_x.shape[1] * h_x.element_size() + h_pos.element_size())
+    h2d = h2d_copied + h2d_in_place
     d2h = h_total.nbytes + h_cuo.nbytes
 
     wm = work_model(inp, G)
@@ -702,6 +723,13 @@ def run_ours(args, inp, w, rank, world):
         clocks=clk,
         e2e=(dict(value=world * inp.total_tokens / e2e_s, unit=UNIT, h2d_bytes_per_step=h2d,
                   d2h_bytes_per_step=d2h, ms_per_step=e2e_s * 1e3,
+                  h2d_copied_bytes=h2d_copied, h2d_read_in_place_bytes=h2d_in_place,
+                  inputs="q, k, cu_seqlens copied from pinned host memory; x and pos read in "
+                         "place from pinned host memory by the compaction (kept rows only); "
+                         "one untimed step before the timed ones",
+                  copy_all_rows=dict(value=world * inp.total_tokens / e2e_copy_s,
+                                     ms_per_step=e2e_copy_s * 1e3,
+                                     h2d_bytes_per_step=h2d_copied + h_x.nbytes + h_pos.nbytes),
                   h2d_copy_gbs={n: round(v, 1) for n, v in h2d_gbs.items()})
              if e2e_s else None),
         gpu_launches=K * sp.launches_per_step(),

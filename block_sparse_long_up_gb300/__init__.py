@@ -107,6 +107,23 @@ def _need(t, name, dtype, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _need_rows(t, name, dtype, device):
+    """x or pos of a compaction: a CUDA tensor on `device`, or a pinned (page-
+    locked) host tensor, which the kernel reads in place through unified
+    addressing (only the kept rows cross the host link)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        _need(t, name, dtype, device)
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+
+
 def _check(where, status):
     if status != 0:
         raise UpError(where, status)
@@ -319,12 +336,13 @@ def compact(x, pos, cu_seqlens, G, keep, cu_blocks, x_out=None, pos_out=None,
             cu_seqlens_out=None, src_idx=None, total_kept=None, workspace=None, stream=None,
             want_src_idx=True):
     """Gather kept rows.  Outputs are sized for keeping everything; the true
-    row count is total_kept (int32 [1], on the device)."""
-    _need(x, "x", torch.bfloat16)
-    dev = x.device
-    _need(pos, "pos", torch.int32, dev)
+    row count is total_kept (int32 [1], on the device).  x and pos may be
+    pinned host tensors: the kernel then reads the kept rows in place."""
+    _need(keep, "keep", torch.uint8)
+    dev = keep.device
+    _need_rows(x, "x", torch.bfloat16, dev)
+    _need_rows(pos, "pos", torch.int32, dev)
     _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
-    _need(keep, "keep", torch.uint8, dev)
     _need(cu_blocks, "cu_blocks", torch.int32, dev)
     total, hidden = x.shape
     B = cu_seqlens.numel() - 1

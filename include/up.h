@@ -254,6 +254,10 @@ up_status up_select_blocks(const float *scores, const int32_t *cu_blocks,
  *
  *   x               bf16 [total_tokens, hidden], 16-byte aligned; hidden % 8 == 0.
  *   pos             int32 [total_tokens].
+ *                   x and pos may be device memory, or pinned (page-locked) host
+ *                   memory that the device addresses through unified addressing
+ *                   (cudaHostAlloc, cudaHostRegister): the kernel then reads only
+ *                   the kept rows across the host link, in place.
  *   keep, cu_blocks as produced above.
  *   x_out           bf16 [capacity, hidden], 16-byte aligned; capacity must be
  *                   >= the number of kept tokens (total_tokens is always enough).

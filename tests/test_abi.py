@@ -238,3 +238,27 @@ def test_compact_noalloc_checks_every_tensor_before_the_library(monkeypatch):
             up.compact_noalloc(**args)
     with pytest.raises(ValueError, match="CUDA"):
         up.compact_noalloc(**good)  # right dtypes and sizes, but host tensors
+
+
+def test_compact_takes_device_or_pinned_host_rows_only(monkeypatch):
+    """x and pos of up.compact may be CUDA tensors or pinned host tensors (read
+    in place by the kernel); an ordinary host tensor raises before the C
+    library is reached.  (The pinned case needs a GPU; see the GPU tests.)"""
+    import torch
+
+    def no_library():
+        raise AssertionError("the C library was reached")
+
+    monkeypatch.setattr(up, "lib", no_library)
+    T, H, G = 128, 16, 64
+    rows = torch.zeros(T, H, dtype=torch.bfloat16)
+    pos = torch.zeros(T, dtype=torch.int32)
+    with pytest.raises(ValueError, match="pinned host tensor"):
+        up._need_rows(rows, "x", torch.bfloat16, None)
+    with pytest.raises(ValueError, match="pinned host tensor"):
+        up._need_rows(pos, "pos", torch.int32, None)
+    with pytest.raises(TypeError, match="x must be"):
+        up._need_rows(rows.float(), "x", torch.bfloat16, None)
+    with pytest.raises(ValueError, match="CUDA"):  # the keep flags must be on a GPU
+        up.compact(rows, pos, torch.tensor([0, T], dtype=torch.int32), G,
+                   torch.zeros(2, dtype=torch.uint8), torch.tensor([0, 2], dtype=torch.int32))

@@ -170,6 +170,42 @@ def test_compact_random_keep(hidden):
         assert np.array_equal(xo, ox)
 
 
+@pytest.mark.parametrize("G,lens", [
+    (32, [130, 0, 64, 1, 1000, 63]),          # one kernel
+    (16, [200000, 0, 77, 100003]),            # index kernel + gather (> 16384 blocks)
+])
+def test_compact_reads_pinned_host_rows_in_place(G, lens):
+    """x and pos in pinned host memory: the compaction reads the kept rows in
+    place (unified addressing) and gives the oracle's output, bit for bit the
+    same as from device copies of x and pos."""
+    rng = np.random.default_rng(len(lens))
+    cu = np.zeros(len(lens) + 1, np.int32)
+    cu[1:] = np.cumsum(lens)
+    nbs = [(L + G - 1) // G for L in lens]
+    cb = np.zeros(len(lens) + 1, np.int32)
+    cb[1:] = np.cumsum(nbs)
+    T, hidden = int(cu[-1]), 64
+    x_bits = rng.integers(0, 1 << 16, size=(T, hidden), dtype=np.uint16)
+    pos = rng.integers(-5, 1 << 30, size=T).astype(np.int32)
+    keep = (rng.random(int(cb[-1])) < 0.3).astype(np.uint8)
+    x_host = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    pos_host = torch.from_numpy(pos).pin_memory()
+    keep_d, cu_d, cb_d = (torch.from_numpy(keep).cuda(), to_dev_i32(cu), to_dev_i32(cb))
+    xo, po, cuo, tk, src = up.compact(x_host, pos_host, cu_d, G, keep_d, cb_d)
+    xd, pd, _, tkd, _ = up.compact(x_host.cuda(), pos_host.cuda(), cu_d, G, keep_d, cb_d)
+    torch.cuda.synchronize()
+    n = int(tk.item())
+    ox, opos, ocu, osrc = oracle.compact(x_bits, pos, cu, G, keep, cb)
+    assert n == len(opos) == int(tkd.item())
+    np.testing.assert_array_equal(cuo.cpu().numpy(), ocu)
+    np.testing.assert_array_equal(src[:n].cpu().numpy(), osrc)
+    np.testing.assert_array_equal(po[:n].cpu().numpy(), opos)
+    assert np.array_equal(xo[:n].view(torch.int16).cpu().numpy().view(np.uint16), ox)
+    assert torch.equal(xo[:n].view(torch.int16), xd[:n].view(torch.int16))  # bits (NaNs included)
+    assert torch.equal(po[:n], pd[:n])
+    assert up.get_device_error() == 0
+
+
 @pytest.mark.parametrize("G,lens,seed", [
     (16, [200000, 0, 77, 100003], 1),       # up to 18759 blocks: index kernel + gather
     (64, [3000] * 300 + [1, 5, 70000], 2),  # 303 sequences, up to 15459 blocks: one kernel
