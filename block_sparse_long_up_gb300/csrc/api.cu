@@ -3,10 +3,22 @@
 #include <atomic>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/up.h"
 #include "common.cuh"
 
 namespace {
+
+// A named NVTX range around each public call's host work (argument checks and
+// launches), so a timeline profiler shows the three calls of a step; without
+// a profiler attached a push or pop is a check of a null hook.
+struct CallRange {
+    explicit CallRange(const char *name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
+};
 
 // Sticky device error word (UP_DEVERR_* bits), one per device.
 __device__ unsigned int g_up_device_error;
@@ -283,6 +295,7 @@ up_status up_score_blocks(const void *q_last, const void *k, const int32_t *cu_s
                           int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
                           int G, float *scores, int32_t *cu_blocks, void *workspace,
                           size_t workspace_bytes, up_stream_t stream) {
+    const CallRange range("up_score_blocks");
     return score_impl(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n, G, Hq,
                       PagedKeys{}, scores, cu_blocks, workspace, workspace_bytes, stream);
 }
@@ -291,6 +304,7 @@ up_status up_score_blocks_shard(const void *q_last, const void *k, const int32_t
                                 int num_seqs, int64_t total_tokens, int Hq, int Hk, int d, int n,
                                 int G, int Hq_total, float *scores, int32_t *cu_blocks,
                                 void *workspace, size_t workspace_bytes, up_stream_t stream) {
+    const CallRange range("up_score_blocks_shard");
     if (Hq_total < Hq || Hq_total < 1) return UP_ERR_INVALID_ARG;
     return score_impl(q_last, k, cu_seqlens, num_seqs, total_tokens, Hq, Hk, d, n, G, Hq_total,
                       PagedKeys{}, scores, cu_blocks, workspace, workspace_bytes, stream);
@@ -302,6 +316,7 @@ up_status up_score_blocks_paged(const void *q_last, const void *k_pages, int64_t
                                 int Hq, int Hk, int d, int n, int G, float *scores,
                                 int32_t *cu_blocks, void *workspace, size_t workspace_bytes,
                                 up_stream_t stream) {
+    const CallRange range("up_score_blocks_paged");
     if (!block_table || page_size < 128 || page_size % 128 != 0 || num_pages < 1 ||
         max_pages < 1 || Hk < 1 || num_pages * (int64_t)Hk * page_size >= ((int64_t)1 << 31))
         return UP_ERR_INVALID_ARG;
@@ -317,6 +332,7 @@ up_status up_score_blocks_paged(const void *q_last, const void *k_pages, int64_t
 up_status up_select_topp(const float *scores, const int32_t *cu_blocks,
                          const int32_t *cu_seqlens, int num_seqs, int G, double p,
                          uint8_t *keep, int32_t *kept_tokens, up_stream_t stream) {
+    const CallRange range("up_select_topp");
     if (num_seqs < 0 || G < 1 || !(p > 0.0)) return UP_ERR_INVALID_ARG;
     if (!valid_G(G)) return UP_ERR_UNSUPPORTED;
     if (num_seqs > 0 && (!scores || !cu_blocks || !cu_seqlens || !keep || !kept_tokens))
@@ -335,6 +351,7 @@ up_status up_select_blocks(const float *scores, const int32_t *cu_blocks,
                            const int32_t *cu_seqlens, int num_seqs, int G, up_select_mode mode,
                            double p, int k, uint32_t flags, uint8_t *keep, int32_t *kept_tokens,
                            up_stream_t stream) {
+    const CallRange range("up_select_blocks");
     if (num_seqs < 0 || G < 1 || (flags & ~UP_SELECT_KEEP_LAST) != 0) return UP_ERR_INVALID_ARG;
     if (mode == UP_SELECT_TOP_P) {
         if (!(p > 0.0)) return UP_ERR_INVALID_ARG;
@@ -358,6 +375,7 @@ up_status up_select_blocks(const float *scores, const int32_t *cu_blocks,
 
 up_status up_block_csr(const uint8_t *keep, const int32_t *cu_blocks, int num_seqs,
                        int32_t *indptr, int32_t *indices, up_stream_t stream) {
+    const CallRange range("up_block_csr");
     if (num_seqs < 0 || !keep || !cu_blocks || !indptr || !indices) return UP_ERR_INVALID_ARG;
     DeviceState *ds = nullptr;
     up_status st = device_state(&ds);
@@ -378,6 +396,7 @@ up_status up_compact(const void *x, const int32_t *pos, int hidden, const int32_
                      const int32_t *cu_blocks, void *x_out, int32_t *pos_out,
                      int32_t *cu_seqlens_out, int32_t *src_idx, int32_t *total_kept,
                      void *workspace, size_t workspace_bytes, up_stream_t stream) {
+    const CallRange range("up_compact");
     if (num_seqs < 0 || total_tokens < 0 || total_tokens > INT32_MAX || hidden < 1 || G < 1)
         return UP_ERR_INVALID_ARG;
     if (!valid_G(G)) return UP_ERR_UNSUPPORTED;

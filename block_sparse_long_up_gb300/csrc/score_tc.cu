@@ -22,8 +22,10 @@
 //   warp 2      Q producer: TMA loads of each pair's Q tiles (one 3-D box of
 //               g heads x 128/g queries x 64 dims per tile and panel);
 //   warps 1, 3  MMA issuers, one per TMEM buffer: S = Q K^T as M=128, N=128
-//               tcgen05.mma chains.  The tensor pipe's issue queue is shallow,
-//               so the bookkeeping of one issuer (barrier waits, commits) runs
+//               tcgen05.mma chains, each K slice issued to the pair's two
+//               tiles in turn (consecutive MMAs never share an accumulator).
+//               The whole warp walks the loop and one elected lane issues, so
+//               the bookkeeping of one issuer (barrier waits, commits) runs
 //               while the other one's MMAs keep the pipe busy (head_dim 256:
 //               each K panel is multiplied and released as soon as it lands);
 //   warps 4-11  two softmax warpgroups; warpgroup e owns tile e of each pair.
