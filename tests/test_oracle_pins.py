@@ -400,17 +400,34 @@ def test_compact_invariants(seed):
     np.testing.assert_array_equal(pos_out, pos[src])
     # source rows strictly increase: original order is kept
     assert np.all(np.diff(src) > 0)
-    # exactly the rows of kept blocks appear
-    want = []
-    for s, L in enumerate(lens):
-        for b in range(int(cb[s + 1] - cb[s])):
-            if keep[cb[s] + b]:
-                want.extend(range(cu[s] + b * G, cu[s] + min(L, (b + 1) * G)))
-    np.testing.assert_array_equal(src, want)
+    # exactly the rows of kept blocks appear: a per-token mask, each token
+    # looking up its own block's flag (token-centric, where the oracle walks
+    # the blocks)
+    tok = np.arange(int(cu[-1]))
+    seq = np.searchsorted(cu, tok, side="right") - 1
+    mask = keep[cb[seq] + (tok - cu[seq]) // G].astype(bool)
+    np.testing.assert_array_equal(src, np.nonzero(mask)[0])
+    np.testing.assert_array_equal(np.diff(cu_out), np.bincount(seq[mask], minlength=len(lens)))
     # cu_out is monotone, and positions strictly increase within each output sequence
     assert np.all(np.diff(cu_out) >= 0) and cu_out[-1] == len(src)
     for s in range(len(lens)):
         assert np.all(np.diff(pos_out[cu_out[s]:cu_out[s + 1]]) > 0)
+
+
+def test_compact_hand_example():
+    """Two sequences of 5 and 3 tokens, G = 2: blocks {0,1} {2,3} {4} and
+    {5,6} {7}; keeping blocks 0 and 2 of the first and block 1 of the second
+    keeps tokens 0, 1, 4 and 7, positions gathered unchanged."""
+    cu = np.array([0, 5, 8], np.int32)
+    cb = np.array([0, 3, 5], np.int32)
+    keep = np.array([1, 0, 1, 0, 1], np.uint8)
+    x = np.arange(8 * 8, dtype=np.uint16).reshape(8, 8)
+    pos = np.array([10, 11, 12, 13, 14, 0, 1, 2], np.int32)
+    x_out, pos_out, cu_out, src = oracle.compact(x, pos, cu, 2, keep, cb)
+    assert src.tolist() == [0, 1, 4, 7]
+    assert pos_out.tolist() == [10, 11, 14, 2]
+    assert cu_out.tolist() == [0, 3, 4]
+    np.testing.assert_array_equal(x_out, x[[0, 1, 4, 7]])
 
 
 def test_block_csr_hand_example_and_round_trip():
