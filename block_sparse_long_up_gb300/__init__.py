@@ -48,7 +48,14 @@ def lib():
         return _lib
     if not os.path.exists(_build.LIB):
         raise RuntimeError(f"{_build.LIB} is missing: build it with block_sparse_long_up_gb300.build()")
-    L = ctypes.CDLL(_build.LIB)
+    _lib = load_library(_build.LIB)
+    return _lib
+
+
+def load_library(path):
+    """Load a build of the C ABI at `path` (the library, or its checked
+    variant from _build.build(checked=True)) with its ctypes signatures."""
+    L = ctypes.CDLL(path)
     P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     L.up_status_string.argtypes = [I]
     L.up_status_string.restype = ctypes.c_char_p
@@ -81,7 +88,6 @@ def lib():
     L.up_measure_ex2_rate.restype = I
     L.up_set_wait_limit.argtypes = [ctypes.c_uint64]
     L.up_set_wait_limit.restype = I
-    _lib = L
     return L
 
 

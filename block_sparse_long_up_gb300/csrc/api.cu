@@ -254,6 +254,9 @@ up_status score_impl(const void *q_last, const void *k, const int32_t *cu_seqlen
     p.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d));
     p.wait_limit = g_wait_limit.load();
     p.err = ds->err;
+    p.part_cap = lay.max_part;
+    p.stat_cap = lay.max_stat;
+    p.scores_cap = lay.max_blocks;
     p.cu_seqlens = cu_seqlens;
     if (num_seqs == 1) {  // the plan's row for the only sequence, from the host's sizes
         const int64_t L = total_tokens, ns = L < n ? L : n;
@@ -427,6 +430,7 @@ up_status up_compact(const void *x, const int32_t *pos, int hidden, const int32_
     a.dst_blk = reinterpret_cast<int32_t *>(ws + lay.dst_blk);
     a.err = ds->err;
     a.max_blocks = total_tokens / G + num_seqs;
+    a.total_tokens = total_tokens;
     a.nb_one = num_seqs == 1 ? (int)((total_tokens + G - 1) / G) : -1;
     a.num_seqs = num_seqs;
     a.G = G;

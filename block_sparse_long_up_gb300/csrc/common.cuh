@@ -73,6 +73,28 @@ struct Counters {
 };
 static_assert(sizeof(Counters) == 64, "Counters is 64 bytes");
 
+// Checked builds (-DUP_CHECK_BOUNDS): every kernel tests the index ranges it
+// writes or reads against its buffers' sizes, sets UP_DEVERR_BOUNDS and skips
+// the access when one falls outside (no trap: the context stays usable).  In
+// the normal build the test is a constant true and compiles away.
+#ifdef UP_CHECK_BOUNDS
+constexpr bool kCheckBounds = true;
+#else
+constexpr bool kCheckBounds = false;
+#endif
+
+// [start, start + len) inside [0, n)?
+__device__ __forceinline__ bool in_range(int64_t start, int64_t len, int64_t n,
+                                         unsigned int *err) {
+    if constexpr (!kCheckBounds) {
+        return true;
+    } else {
+        const bool ok = start >= 0 && len >= 0 && start + len <= n;
+        if (!ok) atomicOr(err, 0x20u);  // UP_DEVERR_BOUNDS
+        return ok;
+    }
+}
+
 constexpr int kRowsPerTile = 128;   // rows of one M tile (TMEM lanes)
 constexpr int kStepKeys = 128;      // keys of one MMA step (N)
 
@@ -135,6 +157,7 @@ struct ScoreParams {
     float scale_log2;  // log2(e) / sqrt(d)
     long long wait_limit;  // bound of every spin-wait of the scoring kernel, SM clock cycles
     unsigned int *err;
+    int64_t part_cap, stat_cap, scores_cap;  // floats in part, in mref/lsum each, in scores
 };
 
 __device__ __forceinline__ int find_seq_by_unit(const SeqInfo *seqs, int B, int u) {
@@ -188,6 +211,7 @@ struct CompactArgs {
     int nb_one;          // one sequence: ceil(total_tokens / G), its block count; else -1
     int num_seqs, G, hidden, rows_per_item, items_per_block;
     int64_t vec_per_row;  // hidden * 2 / 16
+    int64_t total_tokens; // rows of x and pos (and the most rows x_out can need)
 };
 // Compaction kernels: one kernel when max_blocks <= kCompactOneKernelBlocks
 // (every CTA scans the keep flags itself; the scratch is not used), else an

@@ -162,6 +162,8 @@ compact_one_kernel(CompactArgs a) {
     const int np = min(npiece, kOnePieces);  // <= hi - lo <= kOnePieces by the grid size
     for (int i = 0; i < np; ++i) {
         const int4 e = piece[i];
+        if (!in_range(e.x, e.z, a.total_tokens, a.err) || !in_range(e.y, e.z, a.total_tokens, a.err))
+            continue;
         copy_vec<kOneThreads>(a.x + (int64_t)e.x * a.vec_per_row,
                               a.x_out + (int64_t)e.y * a.vec_per_row, (int64_t)e.z * a.vec_per_row);
         for (int r = t; r < e.z; r += kOneThreads) {
@@ -247,6 +249,7 @@ __global__ void __launch_bounds__(kGatherThreads)
 compact_gather_kernel(CompactArgs a) {
     pdl_wait();
     const int K = *a.nkept;
+    if (!in_range(0, K, a.max_blocks, a.err)) return;  // checked builds: the list's length
     const int64_t items = (int64_t)K * a.items_per_block;
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
         const int kb = (int)(it / a.items_per_block);
@@ -255,6 +258,9 @@ compact_gather_kernel(CompactArgs a) {
         const int r0 = q * a.rows_per_item;
         if (r0 >= e.z) continue;
         const int rows = min(e.z - r0, a.rows_per_item);
+        if (!in_range(e.x + r0, rows, a.total_tokens, a.err) ||
+            !in_range(e.y + r0, rows, a.total_tokens, a.err))
+            continue;
         copy_vec<kGatherThreads>(a.x + (int64_t)(e.x + r0) * a.vec_per_row,
                                  a.x_out + (int64_t)(e.y + r0) * a.vec_per_row,
                                  (int64_t)rows * a.vec_per_row);

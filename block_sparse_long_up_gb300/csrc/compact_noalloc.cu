@@ -101,6 +101,7 @@ extern "C" up_status up_compact_noalloc(const void *x, const int32_t *pos, int h
     // the kernels check cu_blocks[num_seqs] against this bound on the device, so
     // a cu_blocks that disagrees with total_tokens never reaches past the array
     a.max_blocks = total_tokens / G + num_seqs;
+    a.total_tokens = total_tokens;
     a.nb_one = num_seqs == 1 ? (int)((total_tokens + G - 1) / G) : -1;
     a.err = up::device_error_word();
     if (!a.err) return UP_ERR_CUDA;

@@ -587,6 +587,14 @@ __device__ void role_softmax(const ScoreParams &p, Shared &sh, uint32_t tmem, in
             rs[pr].a = sq.L - sq.ns + (rs[pr].valid ? tq : 0);
             rs[pr].r = (int64_t)un.j * grows + (int64_t)tq * p.g + h;
             rs[pr].part = p.part + sq.part_off + rs[pr].r;
+            // checked builds: the row's partials and chunk statistics lie in
+            // their buffers (otherwise it stores nothing)
+            if (rs[pr].valid &&
+                !(in_range(sq.part_off + rs[pr].r, (int64_t)(sq.nb - 1) * sq.R + 1, p.part_cap,
+                           p.err) &&
+                  in_range(sq.stat_off + (int64_t)(kSlotsPerChunk * un.c) * sq.R + rs[pr].r, 1,
+                           p.stat_cap, p.err)))
+                rs[pr].valid = false;
             rs[pr].policy = part_policy;
             rs[pr].ref = -INFINITY;
             rs[pr].lsum = 0.f;
@@ -771,7 +779,10 @@ __device__ void epilogue_rows(const ScoreParams &p) {
         const int64_t r = (row_ok ? gr : r0) - sq.row_off;
         float *mref = p.mref + sq.stat_off + r;
         const float *lsum = p.lsum + sq.stat_off + r;
-        const int nch = row_ok ? sq.nchunks : 0;
+        // checked builds: the row's chunk statistics lie in their buffers
+        const bool st_ok = !row_ok || in_range(sq.stat_off + r, (int64_t)(sq.nchunks - 1) * sq.R + 1,
+                                               p.stat_cap, p.err);
+        const int nch = row_ok && st_ok ? sq.nchunks : 0;
         float M = -INFINITY, l = 0.f;
         // this lane's chunks c = sub + kRowLanes * k; the first kEpiChunks of
         // them stay in registers for the weights
@@ -849,6 +860,15 @@ __device__ void epilogue_blocks(const ScoreParams &p, float (*red)[NT / 32]) {
         const int nbat = min(min(kEpiBlocks, hi - gb), min(sq.nb - b, (b / bpc + 1) * bpc - b));
         const float *wr = p.mref + sq.stat_off + (int64_t)block_slot(b, p.G, p.C) * sq.R;
         const float *pt = p.part + sq.part_off + (int64_t)b * sq.R;
+        // checked builds: the batch's partials, weights and scores lie in their
+        // buffers (the test is the same in every thread of the CTA)
+        if (!(in_range(sq.part_off + (int64_t)b * sq.R, (int64_t)nbat * sq.R, p.part_cap, p.err) &&
+              in_range(sq.stat_off + (int64_t)block_slot(b, p.G, p.C) * sq.R, sq.R, p.stat_cap,
+                       p.err) &&
+              in_range(gb, nbat, p.scores_cap, p.err))) {
+            gb += nbat;
+            continue;
+        }
         float acc[kEpiBlocks];
 #pragma unroll
         for (int k = 0; k < kEpiBlocks; ++k) acc[k] = 0.f;
@@ -950,7 +970,12 @@ __device__ void fallback_tiles(const ScoreParams &p, unsigned char *smem) {
         // row tid of the tile: query t = mt * tpt + tid / g of query head j * g + h
         const int tl = tid / p.g, h = tid - tl * p.g;
         const int t = mt * p.tpt + tl;
-        const bool valid = row_thread && tid < p.g * p.tpt && t < sq.ns;
+        const bool valid = row_thread && tid < p.g * p.tpt && t < sq.ns &&
+                           in_range(sq.part_off + (int64_t)j * grows + (int64_t)t * p.g + h,
+                                    (int64_t)(sq.nb - 1) * sq.R + 1, p.part_cap, p.err) &&
+                           in_range(sq.stat_off + (int64_t)(kSlotsPerChunk * c) * sq.R +
+                                        (int64_t)j * grows + (int64_t)t * p.g + h,
+                                    1, p.stat_cap, p.err);
         const int a = sq.L - sq.ns + (valid ? t : 0);
         const int64_t r = (int64_t)j * grows + (int64_t)t * p.g + h;
         __syncthreads();

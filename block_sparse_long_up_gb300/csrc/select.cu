@@ -297,6 +297,11 @@ select_kernel(const float *__restrict__ scores, const int32_t *__restrict__ cu_b
         }
         return;
     }
+    // checked builds: this sequence's flags lie inside the batch's [0, cu_blocks[B])
+    if (!in_range(b0, nb, cu_blocks[gridDim.x], err)) {
+        if (threadIdx.x == 0) kept_tokens[s] = 0;
+        return;
+    }
     const bool all = keep_all != 0, unit = unit_mass != 0, last = keep_last != 0;
     if (nb <= kSelThreads) select_seq<1>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);
     else if (nb <= 2 * kSelThreads) select_seq<2>(scores, b0, nb, L, G, P, unit, all, last, keep, kept_tokens, s, sh);

@@ -62,6 +62,8 @@ typedef enum {
 #define UP_DEVERR_TIMEOUT 0x4u         /* a bounded wait inside a kernel gave up */
 #define UP_DEVERR_BAD_PAGE 0x8u        /* a page index outside [0, num_pages) (read as zeros) */
 #define UP_DEVERR_BAD_CU_BLOCKS 0x10u  /* compaction: cu_blocks[num_seqs] < 0 or > total_tokens/G + num_seqs */
+#define UP_DEVERR_BOUNDS 0x20u         /* checked builds only (compiled with -DUP_CHECK_BOUNDS): an index
+                                          range outside its buffer; the access was skipped */
 
 /* Largest nb_s that the selection calls rank on chip (1M tokens at G = 64). */
 #define UP_SELECT_MAX_BLOCKS 16384

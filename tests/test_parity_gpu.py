@@ -628,3 +628,47 @@ def test_select_keep_last_option(mode):
     for s in range(len(lens)):
         if nbs[s]:
             assert keep[cb[s + 1] - 1] == 1
+
+
+def test_checked_build_matches_the_oracle_with_no_bounds_miss(monkeypatch):
+    """The checked build (-DUP_CHECK_BOUNDS: every kernel tests the index ranges
+    it reads and writes, and reports a miss through UP_DEVERR_BOUNDS instead of
+    trapping) runs the whole path on shapes chosen for their edges -- ragged
+    tiles and blocks, empty and one-token sequences, every head_dim, G = 16
+    and 256, paged keys, the compaction's index + gather path -- and must give
+    the oracle's results with no error bit set."""
+    checked = up.load_library(up._build.build(checked=True))
+    monkeypatch.setattr(up, "_lib", checked)
+    assert up.get_device_error() == 0
+    for lens, Hq, Hk, d, n, G, p in [
+            ([300, 129, 4100], 4, 1, 64, 16, 256, 0.9),
+            ([5, 1, 0, 129], 4, 4, 64, 128, 32, 0.99),
+            ([9000], 12, 4, 128, 48, 16, 0.999),
+            ([2048], 16, 2, 256, 100, 128, 0.9)]:
+        inp = synth.make_inputs(lens, Hq, Hk, d, n, 0.05, gain=5.0, hidden=64,
+                                seed=sum(lens) + d)
+        full_check(inp, n, G, p)
+        assert up.get_device_error() == 0, (lens, d, G)
+    # paged keys
+    inp = synth.make_inputs([3000, 700], 8, 2, 128, 64, 0.05, gain=5.0, hidden=64, seed=5)
+    pool, table = _paged(inp, 256, 3, np.random.default_rng(6))
+    q, cu = to_dev_bf16(inp.q_last), to_dev_i32(inp.cu_seqlens)
+    psc, pcb = up.score_blocks_paged(q, to_dev_bf16(pool), torch.from_numpy(table).cuda(), cu,
+                                     inp.total_tokens, 64, 64)
+    sc, cb = up.score_blocks(q, to_dev_bf16(inp.k), cu, 64, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(psc[: int(cb[-1])], sc[: int(cb[-1])])
+    assert up.get_device_error() == 0
+    # the compaction's two-kernel path (more than 16384 possible blocks)
+    G, lens = 16, [200000, 0, 77, 100003]
+    rng = np.random.default_rng(9)
+    cu_np = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cb_np = np.concatenate([[0], np.cumsum([(L + G - 1) // G for L in lens])]).astype(np.int32)
+    x = rng.integers(0, 1 << 16, size=(int(cu_np[-1]), 8), dtype=np.uint16)
+    pos = np.arange(int(cu_np[-1]), dtype=np.int32)
+    keep = (rng.random(int(cb_np[-1])) < 0.3).astype(np.uint8)
+    xo, po, cuo, src, T = gpu_compact(x, pos, cu_np, G, keep, cb_np)
+    ox, opos, ocu, osrc = oracle.compact(x, pos, cu_np, G, keep, cb_np)
+    assert T == len(opos) and np.array_equal(xo, ox)
+    np.testing.assert_array_equal(src, osrc)
+    assert up.get_device_error() == 0
