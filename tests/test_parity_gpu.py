@@ -42,6 +42,19 @@ def test_small_shapes(lens, Hq, Hk, d, n, G, p, gain):
     full_check(inp, n, G, p)
 
 
+@pytest.mark.parametrize("lens,Hq,Hk,d,n,G,p", [
+    ([3000, 700], 16, 1, 128, 1024, 64, 0.95),   # n = 1024 (the largest window), g = 16, L < n
+    ([2000], 32, 2, 64, 1024, 32, 0.9),          # g = 16 at head_dim 64: 128 row tiles per head
+    ([1500, 1], 48, 3, 256, 1024, 128, 0.99),    # g = 16 at head_dim 256, a one-token sequence
+])
+def test_largest_window_and_group(lens, Hq, Hk, d, n, G, p):
+    """The API's largest query window (n = 1024) and GQA group (Hq / Hk = 16):
+    a tile then holds 8 queries of 16 heads, a KV head has up to 128 row tiles,
+    and sequences shorter than the window use all of their tokens as queries."""
+    inp = synth.make_inputs(lens, Hq, Hk, d, n, 0.05, gain=5.0, hidden=32, seed=sum(lens) + n)
+    full_check(inp, n, G, p)
+
+
 @pytest.mark.parametrize("gain", [5.0, None])
 def test_gqa8x2_d64_4k_workload(gain):
     inp = synth.make_workload("gqa8x2_d64_4k", gain=gain)
