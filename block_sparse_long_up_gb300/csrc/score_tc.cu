@@ -85,9 +85,9 @@ struct Cfg {
     static constexpr int kStagesFit = (kSmemBudget - 1024 - kQBufs * kQBytes) / kPanelBytesK;
     static constexpr int kStages = kStagesFit < kMaxStages ? kStagesFit : kMaxStages;
     static constexpr int kSmem = kQBufs * kQBytes + kStages * kPanelBytesK + 1024;
-    // issuers that read one K stage / one Q pair buffer
-    static constexpr int kStageUsers = kPairs == 2 ? 2 : 1;
-    static constexpr int kQUsers = kPairs == 2 ? 1 : 2;
+    // both issuers read every K stage and every Q pair buffer (one tile each)
+    static constexpr int kStageUsers = 2;
+    static constexpr int kQUsers = 2;
     static_assert(kStages >= kPanels, "at least one K step in flight");
     static_assert(kTiles % 2 == 0 && kPairs <= 2, "tile pairs map onto the two TMEM buffers");
     static_assert(kQSlots <= 4, "Q pair buffers");
@@ -237,17 +237,18 @@ done:
         if ((used >> qs) & 1u) mbar_drain(smem_u32(&sh.qfull[qs]), ((parity >> qs) & 1u) ^ 1u);
 }
 
-// MMA issuer w (0 or 1) issues every MMA into TMEM buffer w.  Slot order (the
-// softmax warpgroups follow the same one): for each unit, each K step, each
-// pair holding queries.  head_dim <= 128: pair p uses buffer p, and both issuers
-// walk every K stage (waiting for it and releasing it, with or without MMAs) so
-// a stage is refilled only after both have released it.  head_dim 256 (one
-// pair): buffer = parity of the CTA-wide K step count, and each stage is used
-// and released by that step's issuer alone.
-// The whole warp walks the loop, so the control flow and the descriptors are
-// warp-uniform, and one elected lane issues the MMAs and commits: a lone
-// thread's instructions, competing with two softmax warps on its SM
-// sub-partition, issued one M128 x N128 MMA every ~107 cycles (64 at full rate).
+// MMA issuer w (0 or 1) issues the MMAs of tile w of every pair, so both
+// issuers fill each TMEM buffer together, one accumulator each.  Slot order
+// (the softmax warpgroups follow the same one): for each unit, each K step,
+// each pair holding queries; head_dim <= 128: pair p uses buffer p; head_dim
+// 256 (one pair): buffer = parity of the CTA-wide K step count.  Both issuers
+// walk every K stage and Q pair buffer and release each after their last MMA
+// on it, and each commits once to the buffer's full barrier.
+// Two instruction streams keep the tensor pipe fed while the softmax warps
+// load their sub-partitions' issue slots: one issuer alternating two
+// accumulators got one M128 x N128 MMA per ~104 cycles under the softmax's
+// load, two issuers ~65 (the full rate).  The whole warp walks the loop
+// (warp-uniform control flow and descriptors) and one elected lane issues.
 template <int D>
 __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_t *kbuf,
                          uint32_t tmem, int units, int w) {
@@ -255,127 +256,98 @@ __device__ void role_mma(const ScoreParams &p, Shared &sh, uint8_t *qbuf, uint8_
     constexpr uint32_t idesc = idesc_bf16_f32(kRowsPerTile, kStepKeys);
     volatile int *abort = &sh.abort;
     const bool leader = elect_one();
-    uint32_t it = 0, gstep = 0, tuse = 0;  // K panels, K steps, uses of TMEM buffer w
+    uint32_t it = 0, gstep = 0;
+    uint32_t tuse = 0u;  // bit b: parity of this issuer's uses of TMEM buffer b so far
     uint32_t qpar = 0u;  // bit qs: parity of the Q loads into pair buffer qs so far
-    const uint32_t d_base = tmem + (uint32_t)(w * kBufCols);
     const uint32_t kbase = smem_u32(kbuf), qbase = smem_u32(qbuf);
     uint32_t ui = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++ui) {
         Unit un;
         decode_unit<D>(p, u, un);
         const int qb = (ui % C::kQBufs) * C::kPairs;
-        const int qs = qb + (C::kPairs == 2 ? w : 0);  // the pair buffer this issuer reads
-        const bool pair_ok = (C::kPairs == 2 ? w : 0) < un.npairs;
-        bool q_ready = false;
+        uint32_t q_ready = 0u;  // bit pr: pair pr's Q seen loaded
         for (int t = 0; t < un.nsteps; ++t, ++gstep) {
             const uint32_t it0 = it;
             it += C::kPanels;
-            if constexpr (C::kPairs == 1) {
-                // head_dim 256: one pair, steps alternate between the issuers
-                // (buffer = step parity) and a stage is used by its step's
-                // issuer alone.  A step is four K panels and the ring holds six,
-                // so the ring's turnover, not the tensor pipe, sets the pace:
-                // each panel is multiplied as soon as it lands and released right
-                // after its MMAs, so a stage is held ~0.3 us instead of a step.
-                if ((gstep & 1u) != (uint32_t)w) continue;  // the other issuer's step
-                if (!q_ready) {
-                    if (!mbar_wait_warp(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort,
-                                        p.wait_limit))
-                        goto out;
-                    q_ready = true;
-                }
-                if (!mbar_wait_warp(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort, p.wait_limit))
-                    goto out;
-                tc_fence_after();
-#pragma unroll 1
-                for (int pn = 0; pn < C::kPanels; ++pn) {
-                    const uint32_t i = it0 + pn;
-                    const uint32_t st = i % C::kStages;
-                    if (!mbar_wait_warp(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort,
-                                        p.wait_limit))
-                        goto out;
-                    tc_fence_after();
-                    const uint64_t bd = smem_desc_sw128(kbase + st * kPanelBytesK);
-                    const uint32_t qp = qbase + qs * C::kQPairBytes + pn * kPanelBytesQ;
-                    const uint64_t ad0 = smem_desc_sw128(qp), ad1 = smem_desc_sw128(qp + C::kQTileBytes);
-                    if (leader) {
-                        // the two tiles' accumulators alternate, so consecutive
-                        // MMAs never wait on each other's accumulation
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {  // 4 x K=16 per 64-wide panel (32 B)
-                            mma_bf16(d_base, ad0 + 2 * ks, bd + 2 * ks, idesc, (pn | ks) != 0);
-                            mma_bf16(d_base + (uint32_t)kStepKeys, ad1 + 2 * ks, bd + 2 * ks, idesc,
-                                     (pn | ks) != 0);
-                        }
-                        mma_commit(smem_u32(&sh.kempty[st]));
-                    }
-                    __syncwarp();
-                }
-                if (leader) mma_commit(smem_u32(&sh.tfull[w]));
-                __syncwarp();
-                ++tuse;
-            } else {
-                // head_dim <= 128: pair w uses buffer w, and both issuers walk
-                // every K stage.  Every K panel of the step (and the Q tiles) are
-                // in shared memory before the first MMA, and the stage releases
-                // come after the last: the issue queue is shallow, so a barrier
-                // check or a commit between two MMAs of the buffer fill leaves the
-                // tensor pipe idle.  These checks come before the wait for the
-                // TMEM buffer, while the softmax warpgroups still hold it (the ring
-                // runs steps ahead, so they almost never block); the fill starts
-                // as soon as the buffer is free.
+            if constexpr (C::kPairs == 2) {
+                // head_dim <= 128: every K panel of the step is in shared memory
+                // before the first MMA; the stage releases come after the last
                 for (int pn = 0; pn < C::kPanels; ++pn) {
                     const uint32_t i = it0 + pn;
                     if (!mbar_wait_warp(smem_u32(&sh.kfull[i % C::kStages]), (i / C::kStages) & 1,
                                         abort, p.wait_limit))
                         goto out;
                 }
-                if (pair_ok) {
-                    if (!q_ready) {
-                        if (!mbar_wait_warp(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort,
-                                            p.wait_limit))
-                            goto out;
-                        q_ready = true;
-                    }
-                    if (!mbar_wait_warp(smem_u32(&sh.tempty[w]), (tuse & 1) ^ 1, abort,
+            }
+            for (int pr = 0; pr < C::kPairs; ++pr) {
+                if (pr >= un.npairs) break;
+                const int qs = qb + pr;
+                const int buf = C::kPairs == 2 ? pr : (int)(gstep & 1u);
+                if (!((q_ready >> pr) & 1u)) {
+                    if (!mbar_wait_warp(smem_u32(&sh.qfull[qs]), (qpar >> qs) & 1u, abort,
                                         p.wait_limit))
                         goto out;
-                    tc_fence_after();
+                    q_ready |= 1u << pr;
+                }
+                if (!mbar_wait_warp(smem_u32(&sh.tempty[buf]), ((tuse >> buf) & 1u) ^ 1u, abort,
+                                    p.wait_limit))
+                    goto out;
+                tuse ^= 1u << buf;
+                tc_fence_after();
+                const uint32_t d_tile = tmem + (uint32_t)(buf * kBufCols + w * kStepKeys);
+                const uint32_t qt = qbase + qs * C::kQPairBytes + w * C::kQTileBytes;
+#pragma unroll 1
+                for (int pn = 0; pn < C::kPanels; ++pn) {
+                    const uint32_t i = it0 + pn;
+                    const uint32_t st = i % C::kStages;
+                    if constexpr (C::kPairs == 1) {
+                        // head_dim 256: each panel is multiplied as soon as it
+                        // lands and released right after (the ring holds six
+                        // panels of a four-panel step)
+                        if (!mbar_wait_warp(smem_u32(&sh.kfull[st]), (i / C::kStages) & 1, abort,
+                                            p.wait_limit))
+                            goto out;
+                        tc_fence_after();
+                    }
+                    const uint64_t bd = smem_desc_sw128(kbase + st * kPanelBytesK);
+                    const uint64_t ad = smem_desc_sw128(qt + pn * kPanelBytesQ);
                     if (leader) {
 #pragma unroll
-                        for (int pn = 0; pn < C::kPanels; ++pn) {
-                            const uint32_t st = (it0 + pn) % C::kStages;
-                            const uint64_t bd = smem_desc_sw128(kbase + st * kPanelBytesK);
-                            const uint32_t qp = qbase + qs * C::kQPairBytes + pn * kPanelBytesQ;
-                            const uint64_t ad0 = smem_desc_sw128(qp);
-                            const uint64_t ad1 = smem_desc_sw128(qp + C::kQTileBytes);
-                            // the two tiles' accumulators alternate, so consecutive
-                            // MMAs never wait on each other's accumulation (an
-                            // M128 x N128 MMA chained on one accumulator took
-                            // ~100 cycles, alternating ones ~65)
-#pragma unroll
-                            for (int ks = 0; ks < 4; ++ks) {  // 4 x K=16 per 64-wide panel
-                                mma_bf16(d_base, ad0 + 2 * ks, bd + 2 * ks, idesc, (pn | ks) != 0);
-                                mma_bf16(d_base + (uint32_t)kStepKeys, ad1 + 2 * ks, bd + 2 * ks,
-                                         idesc, (pn | ks) != 0);
-                            }
-                        }
-                        mma_commit(smem_u32(&sh.tfull[w]));
+                        for (int ks = 0; ks < 4; ++ks)  // 4 x K=16 per 64-wide panel (32 B)
+                            mma_bf16(d_tile, ad + 2 * ks, bd + 2 * ks, idesc, (pn | ks) != 0);
+                        if constexpr (C::kPairs == 1) mma_commit(smem_u32(&sh.kempty[st]));
                     }
                     __syncwarp();
                 }
+                if (leader) mma_commit(smem_u32(&sh.tfull[buf]));
+                __syncwarp();
+            }
+            if constexpr (C::kPairs == 1) {
+                // a step without the pair (no queries) still releases its panels
+                if (un.npairs == 0) {
+                    for (int pn = 0; pn < C::kPanels; ++pn) {
+                        const uint32_t i = it0 + pn;
+                        if (!mbar_wait_warp(smem_u32(&sh.kfull[i % C::kStages]),
+                                            (i / C::kStages) & 1, abort, p.wait_limit))
+                            goto out;
+                        if (leader) mma_commit(smem_u32(&sh.kempty[i % C::kStages]));
+                        __syncwarp();
+                    }
+                }
+            } else {
                 if (leader) {
                     for (int pn = 0; pn < C::kPanels; ++pn)
                         mma_commit(smem_u32(&sh.kempty[(it0 + pn) % C::kStages]));
                 }
                 __syncwarp();
-                if (pair_ok) ++tuse;
             }
         }
-        // the pair buffer is free once this issuer's MMAs on it have completed
-        if ((C::kPairs == 1 || pair_ok) && leader) mma_commit(smem_u32(&sh.qempty[qs]));
-        __syncwarp();
-        for (int pr = 0; pr < un.npairs; ++pr) qpar ^= 1u << (qb + pr);
+        // each pair buffer is free once this issuer's MMAs on it have completed
+        for (int pr = 0; pr < un.npairs; ++pr) {
+            if (leader) mma_commit(smem_u32(&sh.qempty[qb + pr]));
+            __syncwarp();
+            qpar ^= 1u << (qb + pr);
+        }
     }
 out:
     // every MMA issued by this warp has completed once fin fires
@@ -1091,7 +1063,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             mbar_init(smem_u32(&sh.qempty[q]), C::kQUsers);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&sh.tfull[b]), 1);
+            mbar_init(smem_u32(&sh.tfull[b]), 2);  // one commit per issuer
             mbar_init(smem_u32(&sh.tempty[b]), 2 * kEpiThreads);
             mbar_init(smem_u32(&sh.fin[b]), 1);
         }
