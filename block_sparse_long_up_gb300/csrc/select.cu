@@ -29,6 +29,16 @@
 // by comparing itself with the others.  Ties (equal scores) are separated by
 // the index digits.  Five passes at most: score bits 30..19, 18..7, 6..0, then
 // index bits 15..4 and 3..0.
+//
+// Before the passes, one CTA-wide reduction gives the masses (and counts) of
+// the keys with scores >= 2^-8, >= 2^-14 and >= 2^-20 (a sequence's scores sum
+// to 1).  If the keys at or above such a threshold already hold mass >= P,
+// every key below it has mass-before >= P and is dropped; it also ranks after
+// all of them, so leaving it out changes no mass-before of the others: the
+// search runs over the keys at or above the highest threshold that holds P (at
+// attention-like scores a few dozen, which the compare-count finishes without
+// a histogram pass).  Sequences of more than 4096 blocks search all of their
+// keys.
 #include "../../include/up.h"
 #include "common.cuh"
 
@@ -40,6 +50,7 @@ constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBuckets = 4096;
 constexpr int kSmallM = 64;  // keys left in the crossing bucket that a compare-count finishes
+static_assert(16 * kSmallM == kSelThreads, "the compare-count gives each key 16 threads");
 constexpr int kPasses = 5;
 
 struct SelectShared {
@@ -53,7 +64,21 @@ struct SelectShared {
     unsigned long long base, kstar;
     int cross, m, nmem;
     int kept[kSelWarps];
+    unsigned long long fmass[3][kSelWarps];  // threshold filter: per-warp masses and counts
+    unsigned int fcnt[3][kSelWarps];
+    unsigned int fT;                         // the filter's high-word bound (0xFFFFFFFF: none)
+    int fM;                                  // keys it leaves
 };
+
+// High words of the filter's thresholds: score >= 2^-j <=> the rank key's high
+// word (0x7FFFFFFF - score bits) <= 0x7FFFFFFF - ((127 - j) << 23).
+__host__ __device__ constexpr unsigned filter_bound(int j) {
+    return 0x7FFFFFFFu - ((unsigned)(127 - j) << 23);
+}
+constexpr int kFilters = 3;
+__device__ __forceinline__ unsigned filter_threshold(int f) {
+    return f == 0 ? filter_bound(8) : f == 1 ? filter_bound(14) : filter_bound(20);
+}
 
 __device__ __forceinline__ unsigned long long rank_key(float score, int idx) {
     // scores are >= 0; -0, NaN and anything not > 0 rank as 0.  The score bits
@@ -138,9 +163,69 @@ __device__ void select_seq(const float *__restrict__ scores, int b0, int nb, int
     auto mass = [&](int i) { return unit_mass ? 1ull : key_fixed(key(i)); };
     unsigned long long kstar = ~0ull;  // keep-all
     if (!keep_all) {
+        // the threshold filter: keys with a high word above T cannot be kept
+        unsigned T = 0xFFFFFFFFu;
+        int m = nb;
+        if constexpr (E <= 4) {  // (longer sequences: registers are short, and they search all keys)
+            unsigned long long fm[kFilters];
+            unsigned fc[kFilters];
+#pragma unroll
+            for (int f = 0; f < kFilters; ++f) {
+                fm[f] = 0ull;
+                fc[f] = 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                if (t + i * kSelThreads >= nb) continue;
+                const unsigned long long mi = mass(i);
+#pragma unroll
+                for (int f = 0; f < kFilters; ++f)
+                    if (khi[i] <= filter_threshold(f)) {
+                        fm[f] += mi;
+                        ++fc[f];
+                    }
+            }
+#pragma unroll
+            for (int f = 0; f < kFilters; ++f) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    fm[f] += __shfl_xor_sync(0xffffffffu, fm[f], o);
+                    fc[f] += __shfl_xor_sync(0xffffffffu, fc[f], o);
+                }
+                if (lane == 0) {
+                    sh.fmass[f][wid] = fm[f];
+                    sh.fcnt[f][wid] = fc[f];
+                }
+            }
+            __syncthreads();
+            if (wid == 0) {
+                unsigned bound = 0xFFFFFFFFu;
+                int left = nb;
+#pragma unroll
+                for (int f = 0; f < kFilters; ++f) {
+                    unsigned long long v = lane < kSelWarps ? sh.fmass[f][lane] : 0ull;
+                    unsigned c = lane < kSelWarps ? sh.fcnt[f][lane] : 0u;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        v += __shfl_xor_sync(0xffffffffu, v, o);
+                        c += __shfl_xor_sync(0xffffffffu, c, o);
+                    }
+                    if (bound == 0xFFFFFFFFu && v >= P) {  // the highest threshold that holds P
+                        bound = filter_threshold(f);
+                        left = (int)c;
+                    }
+                }
+                if (lane == 0) {
+                    sh.fT = bound;
+                    sh.fM = left;
+                }
+            }
+            __syncthreads();
+            T = sh.fT;
+            m = sh.fM;
+        }
         unsigned long long prefix = 0ull, base = 0ull;
         int fixed_from = 64;  // key bits >= fixed_from are those of the crossing bucket
-        int m = nb;
 #pragma unroll 1
         for (int ps = 0; ps < kPasses && m > kSmallM; ++ps) {
             const int shift = pass_shift(ps), nbk = 1 << pass_width(ps);
@@ -155,8 +240,8 @@ __device__ void select_seq(const float *__restrict__ scores, int b0, int nb, int
             for (int i = 0; i < E; ++i) {
                 const int e = t + i * kSelThreads;
                 const unsigned long long k = key(i);
-                const bool member =
-                    e < nb && (fixed_from == 64 || (k >> fixed_from) == (prefix >> fixed_from));
+                const bool member = e < nb && khi[i] <= T &&
+                                    (fixed_from == 64 || (k >> fixed_from) == (prefix >> fixed_from));
                 const int b = member ? (int)((k >> shift) & (unsigned long long)(nbk - 1)) : -1;
                 const unsigned long long fx = member ? mass(i) : 0ull;
                 // Neighbouring blocks often share a bucket (scores of similar
@@ -231,7 +316,8 @@ __device__ void select_seq(const float *__restrict__ scores, int b0, int nb, int
         for (int i = 0; i < E; ++i) {
             const int e = t + i * kSelThreads;
             const unsigned long long k = key(i);
-            if (e < nb && (fixed_from == 64 || (k >> fixed_from) == (prefix >> fixed_from))) {
+            if (e < nb && khi[i] <= T &&
+                (fixed_from == 64 || (k >> fixed_from) == (prefix >> fixed_from))) {
                 const int slot = atomicAdd(&sh.nmem, 1);
                 if (slot < kSmallM) {
                     sh.mkey[slot] = k;
@@ -241,12 +327,18 @@ __device__ void select_seq(const float *__restrict__ scores, int b0, int nb, int
         }
         __syncthreads();
         const int nm = min(sh.nmem, kSmallM);
-        if (t < nm) {
-            const unsigned long long ki = sh.mkey[t];
-            unsigned long long bf = base;
-            for (int j = 0; j < nm; ++j)
-                if (sh.mkey[j] < ki) bf += sh.mfx[j];
-            if (bf < P) atomicMax(&sh.kstar, ki);
+        {
+            // 16 threads per key (kSelThreads = 16 * kSmallM), each summing the
+            // masses of every 16th other key ranked before it
+            const int mi = t >> 4, q = t & 15;
+            const unsigned long long ki = mi < nm ? sh.mkey[mi] : 0ull;
+            unsigned long long bf = 0ull;
+            if (mi < nm)
+                for (int j = q; j < nm; j += 16)
+                    if (sh.mkey[j] < ki) bf += sh.mfx[j];
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) bf += __shfl_xor_sync(0xffffffffu, bf, o);
+            if (mi < nm && q == 0 && base + bf < P) atomicMax(&sh.kstar, ki);
         }
         __syncthreads();
         kstar = sh.kstar;
