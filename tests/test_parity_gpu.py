@@ -685,3 +685,39 @@ def test_checked_build_matches_the_oracle_with_no_bounds_miss(monkeypatch):
     assert T == len(opos) and np.array_equal(xo, ox)
     np.testing.assert_array_equal(src, osrc)
     assert up.get_device_error() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("nb", [40, 1500, 4096])
+def test_select_threshold_filter_edges(nb):
+    """Scores placed at and around the selection's filter thresholds (2^-8,
+    2^-14, 2^-20: exact binary values, their neighbours and the ranges between)
+    with p chosen so that each threshold, or none, is the highest whose keys at
+    or above hold p; top-p and top-k against the oracle on the same fp32 scores."""
+    rng = np.random.default_rng(nb)
+    edges = []
+    for j in (8, 14, 20):
+        t = np.float32(2.0 ** -j)
+        edges += [t, np.nextafter(t, np.float32(1)), np.nextafter(t, np.float32(0))]
+    sc = np.concatenate([np.array(edges, np.float32),
+                         np.float32(2.0) ** -rng.uniform(0, 26, size=nb - len(edges)).astype(np.float32)])
+    sc = rng.permutation(sc / sc.sum()).astype(np.float32).astype(np.float64)
+    G = 64
+    cu = np.array([0, nb * G - 3], np.int32)
+    cb = np.array([0, nb], np.int32)
+    order = np.sort(sc)[::-1]
+    ps = {0.3, 0.9, 0.999, 1.0}
+    for j in (8, 14, 20):  # p right at, just above and just below each threshold's own mass
+        at = float(order[order >= 2.0 ** -j].sum())
+        ps |= {min(at, 1.0), min(np.nextafter(at, 2.0), 1.0), np.nextafter(at, 0.0)}
+    for p in sorted(x for x in ps if x > 0):
+        keep, kt = gpu_select(sc, cb, cu, G, p)
+        ok, okt, ci, ce = oracle.select_topp(sc, cb, cu, G, p)
+        hard, _ = keep_mismatch(keep, ok, ci, ce, p)
+        assert hard == 0, (nb, p)
+    for k in sorted({1, 3, len(edges), nb // 2, nb - 1}):
+        keep, kt = gpu_select_blocks(sc, cb, cu, G, mode="top_k", k=k)
+        ok, okt = oracle.select_topk(sc, cb, cu, G, k)
+        np.testing.assert_array_equal(keep, ok)
+        np.testing.assert_array_equal(kt, okt)
+    assert up.get_device_error() == 0
