@@ -755,7 +755,12 @@ def run_ours(args, inp, w, rank, world):
                               peak=hbm, unit="GB/s",
                               frac=cbytes / (calls["compact"] * 1e-3) / 1e9 / hbm, bytes=cbytes,
                               select_compact_frac=cbytes / (calls["select_compact"] * 1e-3) / 1e9
-                              / hbm),
+                              / hbm,
+                              # select + compact inside the pipelined step: the step's time
+                              # less the scoring call's (plan + scoring kernel), both timed here
+                              in_step_us=(ms_step - calls["score"]) * 1e3,
+                              in_step_frac=(cbytes / ((ms_step - calls["score"]) * 1e-3) / 1e9 / hbm
+                                            if ms_step > calls["score"] else None)),
         kept=dict(tokens=kept, blocks=kept_blocks, blocks_total=wm["blocks"],
                   rho=kept / inp.total_tokens),
     )
